@@ -1,0 +1,306 @@
+/*
+ * fa_ref.c -- FP64 CPU oracle for the exact attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY (see fa_ref.h).  Plain loops in double precision,
+ * no blocking beyond what the blocked form itself states, no fusion.
+ */
+#include "fa_ref.h"
+
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- exact decoding of the input encodings ------------------------------ */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double decode_binary16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)f, -24);                 /* zero / subnormal */
+    else if (e == 31)
+        mag = f ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(1024 + f), e - 25);     /* (1.f) * 2^(e-15) */
+    return sign ? -mag : mag;
+}
+
+/* bfloat16 is the upper half of an IEEE 754 binary32. */
+static double decode_bfloat16(uint16_t b)
+{
+    uint32_t w = (uint32_t)b << 16;
+    float x;
+    memcpy(&x, &w, sizeof x);
+    return (double)x;
+}
+
+static double load(const void* p, int enc, size_t idx)
+{
+    switch (enc) {
+    case FA_REF_ENC_F16:  return decode_binary16(((const uint16_t*)p)[idx]);
+    case FA_REF_ENC_BF16: return decode_bfloat16(((const uint16_t*)p)[idx]);
+    default:              return ((const double*)p)[idx];
+    }
+}
+
+static int bad_args(const void* q, const void* k, const void* v, int enc,
+                    long B, long H, long N, long D)
+{
+    if (!q || !k || !v) return 1;
+    if (B < 1 || H < 1 || N < 1 || D < 1) return 1;
+    if (enc != FA_REF_ENC_F64 && enc != FA_REF_ENC_F16 && enc != FA_REF_ENC_BF16) return 1;
+    return 0;
+}
+
+int fa_ref_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static void set_threads(int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+    else omp_set_num_threads(omp_get_num_procs());
+#else
+    (void)nthreads;
+#endif
+}
+
+/* ---- naive safe softmax, one row ---------------------------------------- */
+
+/* Scores of row i against every key, the row max, the exponentials shifted
+ * by that max, their sum, the weighted sum of values, and the log-sum-exp.
+ * s is scratch of length N. */
+static void naive_row(const void* q, const void* k, const void* v, int enc,
+                      long N, long D, double scale, int causal,
+                      size_t head_base, long i, double* s,
+                      double* o_row, double* lse_out)
+{
+    long nvis = causal ? (i + 1 < N ? i + 1 : N) : N;
+    size_t qrow = head_base + (size_t)i * (size_t)D;
+    for (long d = 0; d < D; ++d) o_row[d] = 0.0;
+    if (nvis <= 0) {
+        *lse_out = -INFINITY;
+        return;
+    }
+    double m = -INFINITY;
+    for (long j = 0; j < nvis; ++j) {
+        size_t krow = head_base + (size_t)j * (size_t)D;
+        double dot = 0.0;
+        for (long d = 0; d < D; ++d)
+            dot += load(q, enc, qrow + d) * load(k, enc, krow + d);
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (long j = 0; j < nvis; ++j) {
+        double p = exp(s[j] - m);
+        size_t vrow = head_base + (size_t)j * (size_t)D;
+        l += p;
+        for (long d = 0; d < D; ++d)
+            o_row[d] += p * load(v, enc, vrow + d);
+    }
+    for (long d = 0; d < D; ++d) o_row[d] /= l;
+    *lse_out = m + log(l);
+}
+
+int fa_ref_naive(const void* q, const void* k, const void* v, int enc,
+                 double* o, double* lse,
+                 long B, long H, long N, long D, double scale, int causal,
+                 int nthreads)
+{
+    if (bad_args(q, k, v, enc, B, H, N, D) || !o || !lse) return -1;
+    set_threads(nthreads);
+    long rows = B * H * N;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!s) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < rows; ++r) {
+            if (!s) continue;
+            long bh = r / N, i = r % N;
+            size_t head_base = (size_t)bh * (size_t)N * (size_t)D;
+            naive_row(q, k, v, enc, N, D, scale, causal, head_base, i, s,
+                      o + (size_t)r * (size_t)D, lse + r);
+        }
+        free(s);
+    }
+    return failed ? -2 : 0;
+}
+
+int fa_ref_naive_rows(const void* q, const void* k, const void* v, int enc,
+                      long B, long H, long N, long D, double scale, int causal,
+                      const long* bh_idx, const long* row_idx, long nrows,
+                      double* o_rows, double* lse_rows, int nthreads)
+{
+    if (bad_args(q, k, v, enc, B, H, N, D) || !bh_idx || !row_idx || !o_rows || !lse_rows)
+        return -1;
+    for (long r = 0; r < nrows; ++r)
+        if (bh_idx[r] < 0 || bh_idx[r] >= B * H || row_idx[r] < 0 || row_idx[r] >= N) return -1;
+    set_threads(nthreads);
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!s) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long r = 0; r < nrows; ++r) {
+            if (!s) continue;
+            size_t head_base = (size_t)bh_idx[r] * (size_t)N * (size_t)D;
+            naive_row(q, k, v, enc, N, D, scale, causal, head_base, row_idx[r], s,
+                      o_rows + (size_t)r * (size_t)D, lse_rows + r);
+        }
+        free(s);
+    }
+    return failed ? -2 : 0;
+}
+
+/* ---- blocked online softmax --------------------------------------------- */
+
+/* One (Q block i0, K/V block j0) update of the running state of one head:
+ *   S      = scale * Q_i K_j^T, with masked entries set to -inf
+ *   m_new  = max(m_old, rowmax S)
+ *   P      = exp(S - m_new)
+ *   corr   = 0 if m_old = -inf, else exp(m_old - m_new)
+ *   l      = l * corr + rowsum P
+ *   O      = O * corr + P V_j
+ *   m      = m_new                                                       */
+static void block_update(const void* q, const void* k, const void* v, int enc,
+                         long N, long D, double scale, int causal, int rescale,
+                         size_t head_base, long i0, long i1, long j0, long j1,
+                         double* m, double* l, double* O, double* s,
+                         long trace_row, double* trace, long trace_cap, long* trace_len)
+{
+    long bc = j1 - j0;
+    for (long i = i0; i < i1; ++i) {
+        size_t qrow = head_base + (size_t)i * (size_t)D;
+        double m_blk = -INFINITY;
+        for (long j = j0; j < j1; ++j) {
+            double sij;
+            if (causal && j > i) {
+                sij = -INFINITY;
+            } else {
+                size_t krow = head_base + (size_t)j * (size_t)D;
+                double dot = 0.0;
+                for (long d = 0; d < D; ++d)
+                    dot += load(q, enc, qrow + d) * load(k, enc, krow + d);
+                sij = scale * dot;
+            }
+            s[j - j0] = sij;
+            if (sij > m_blk) m_blk = sij;
+        }
+        double m_old = m[i];
+        double m_new = m_old > m_blk ? m_old : m_blk;
+        double corr;
+        if (!rescale)
+            corr = 1.0;
+        else
+            corr = isinf(m_old) && m_old < 0 ? 0.0 : exp(m_old - m_new);
+        double l_blk = 0.0;
+        double* o_row = O + (size_t)i * (size_t)D;
+        for (long d = 0; d < D; ++d) o_row[d] *= corr;
+        for (long c = 0; c < bc; ++c) {
+            /* exp(-inf - m_new) is 0 for finite m_new; a row whose every score
+             * so far is -inf keeps p = 0 instead of exp(-inf + inf). */
+            double p = (isinf(s[c]) && s[c] < 0) ? 0.0 : exp(s[c] - m_new);
+            if (p == 0.0) continue;
+            size_t vrow = head_base + (size_t)(j0 + c) * (size_t)D;
+            l_blk += p;
+            for (long d = 0; d < D; ++d) o_row[d] += p * load(v, enc, vrow + d);
+        }
+        l[i] = l[i] * corr + l_blk;
+        m[i] = m_new;
+        if (trace && i == trace_row && *trace_len < trace_cap) {
+            double* t = trace + 4 * (*trace_len);
+            t[0] = (double)j0;
+            t[1] = m_new;
+            t[2] = l[i];
+            t[3] = corr;
+            ++*trace_len;
+        }
+    }
+}
+
+int fa_ref_blocked(const void* q, const void* k, const void* v, int enc,
+                   double* o, double* lse,
+                   long B, long H, long N, long D, double scale, int causal,
+                   long Br, long Bc, int kv_outer, int rescale,
+                   long trace_row, double* trace, long trace_cap, long* trace_len,
+                   long* visited, int nthreads)
+{
+    if (bad_args(q, k, v, enc, B, H, N, D) || !o || !lse || Br < 1 || Bc < 1) return -1;
+    if (trace && (!trace_len || trace_cap < 0)) return -1;
+    if (trace_len) *trace_len = 0;
+    set_threads(nthreads);
+    long BH = B * H;
+    long pairs_head0 = 0;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh) {
+        double* m = (double*)malloc(sizeof(double) * (size_t)N);
+        double* l = (double*)malloc(sizeof(double) * (size_t)N);
+        double* O = (double*)calloc((size_t)N * (size_t)D, sizeof(double));
+        double* s = (double*)malloc(sizeof(double) * (size_t)Bc);
+        if (!m || !l || !O || !s) {
+#pragma omp atomic write
+            failed = 1;
+            free(m); free(l); free(O); free(s);
+            continue;
+        }
+        for (long i = 0; i < N; ++i) { m[i] = -INFINITY; l[i] = 0.0; }
+        size_t head_base = (size_t)bh * (size_t)N * (size_t)D;
+        double* tr = (bh == 0) ? trace : NULL;
+        long pairs = 0;
+        long outer_n = kv_outer ? Bc : Br;
+        long inner_n = kv_outer ? Br : Bc;
+        for (long a0 = 0; a0 < N; a0 += outer_n) {
+            for (long b0 = 0; b0 < N; b0 += inner_n) {
+                long i0 = kv_outer ? b0 : a0;
+                long j0 = kv_outer ? a0 : b0;
+                long i1 = i0 + Br < N ? i0 + Br : N;
+                long j1 = j0 + Bc < N ? j0 + Bc : N;
+                /* every query of the block precedes every key of the block */
+                if (causal && i1 - 1 < j0) continue;
+                ++pairs;
+                block_update(q, k, v, enc, N, D, scale, causal, rescale, head_base,
+                             i0, i1, j0, j1, m, l, O, s, trace_row, tr, trace_cap,
+                             trace_len);
+            }
+        }
+        for (long i = 0; i < N; ++i) {
+            double* dst = o + ((size_t)bh * (size_t)N + (size_t)i) * (size_t)D;
+            const double* src = O + (size_t)i * (size_t)D;
+            if (l[i] > 0.0) {
+                for (long d = 0; d < D; ++d) dst[d] = src[d] / l[i];
+                lse[(size_t)bh * (size_t)N + (size_t)i] = m[i] + log(l[i]);
+            } else {
+                for (long d = 0; d < D; ++d) dst[d] = 0.0;
+                lse[(size_t)bh * (size_t)N + (size_t)i] = -INFINITY;
+            }
+        }
+        if (bh == 0) pairs_head0 = pairs;
+        free(m); free(l); free(O); free(s);
+    }
+    if (visited) *visited = pairs_head0;
+    return failed ? -2 : 0;
+}

@@ -1,0 +1,86 @@
+/*
+ * fa_ref.h -- FP64 CPU oracle for the exact attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the bench may load this library.  It shares no code, header
+ * or constant with the CUDA path, and the CUDA path never calls it.
+ *
+ * What it computes, for every (b, h, i):
+ *     s_ij  = scale * sum_d q[i,d] * k[j,d]        for the visible keys j
+ *     m_i   = max_j s_ij
+ *     O_i   = sum_j exp(s_ij - m_i) v_j / sum_j exp(s_ij - m_i)
+ *     LSE_i = m_i + ln sum_j exp(s_ij - m_i)
+ * "Visible" is every j < N, or j <= i when causal (the mask M_ij = -inf for
+ * j > i of "CUDA FlashAttention: from online softmax to the long-sequence IO
+ * limit", section 1).  A row with no visible key (cannot happen for the square
+ * causal mask with N >= 1) is defined as O = 0, LSE = -inf, never NaN.
+ *
+ * Tensors are [B, H, N, D] row-major and contiguous; LSE is [B, H, N].
+ * Inputs are given in one of three encodings (FA_REF_ENC_*) and are decoded
+ * exactly to double before any arithmetic; outputs are double.
+ *
+ * Every entry point returns 0 on success and a negative value on a bad
+ * argument (null pointer, non-positive size, bad encoding).
+ */
+#ifndef FA_REF_H
+#define FA_REF_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { FA_REF_ENC_F64 = 0, FA_REF_ENC_F16 = 1, FA_REF_ENC_BF16 = 2 };
+
+/* Plain safe-softmax attention, one query row at a time (the naive form of
+ * "Why FlashAttention does not need to store the attention matrix", section
+ * 3.1: subtract the row max, exponentiate, normalise).  OpenMP over rows;
+ * nthreads <= 0 means the OpenMP default. */
+int fa_ref_naive(const void* q, const void* k, const void* v, int enc,
+                 double* o, double* lse,
+                 long B, long H, long N, long D, double scale, int causal,
+                 int nthreads);
+
+/* The same definition evaluated only on selected rows: row r of the output is
+ * query row row_idx[r] of head bh_idx[r] (bh = b*H + h).  o_rows is
+ * [nrows, D], lse_rows is [nrows]. */
+int fa_ref_naive_rows(const void* q, const void* k, const void* v, int enc,
+                      long B, long H, long N, long D, double scale, int causal,
+                      const long* bh_idx, const long* row_idx, long nrows,
+                      double* o_rows, double* lse_rows, int nthreads);
+
+/* Blocked online-softmax form: running max m, running sum l and an
+ * unnormalised accumulator O per query row, updated once per (Q block, K/V
+ * block) pair with the correction factor exp(m_old - m_new), which is taken
+ * as 0 while m_old is still -inf ("Why FlashAttention does not need to store
+ * the attention matrix", sections 3.2 and 4.1; "FlashAttention algorithm
+ * details", section 4.2.1).  Causal: a block pair whose queries all precede
+ * its keys is skipped (section 4.5 of the first page); elsewhere masked
+ * scores are -inf before the block max.
+ *
+ *   Br, Bc     query / key block sizes (any value >= 1)
+ *   kv_outer   1: outer loop over K/V blocks, inner over Q blocks (the order
+ *              of the first FlashAttention paper, used by the page's script);
+ *              0: outer loop over Q blocks (FlashAttention-2 order)
+ *   rescale    1: the method.  0: force the correction factor to 1 -- a
+ *              deliberately wrong variant used only as a mutation test.
+ *   trace_row  if trace != NULL, every visited block pair that contains query
+ *              row trace_row of head 0 appends (j0, m_new, l_new, corr) to
+ *              trace (4 doubles each, at most trace_cap entries); the number
+ *              of entries written goes to *trace_len.
+ *   visited    if not NULL, receives the number of block pairs computed for
+ *              one head.
+ */
+int fa_ref_blocked(const void* q, const void* k, const void* v, int enc,
+                   double* o, double* lse,
+                   long B, long H, long N, long D, double scale, int causal,
+                   long Br, long Bc, int kv_outer, int rescale,
+                   long trace_row, double* trace, long trace_cap, long* trace_len,
+                   long* visited, int nthreads);
+
+/* Threads the OpenMP runtime would use for nthreads <= 0. */
+int fa_ref_max_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_REF_H */
