@@ -1,0 +1,377 @@
+"""Benchmark of the exact attention forward pass (one JSON line on stdout).
+
+One step = one fa_fwd call over the whole workload (every step of the path:
+Q-tile loads, K/V streaming, S = QK^T, masking, online softmax, rescale,
+O += PV, the O / l and LSE epilogue).  Default workload: B=1, H=32, N=8192,
+D=128, causal, fp16 -- the configuration the throughput target is quoted on.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Metric: attention forward TFLOP/s with the causal-adjusted FLOP model
+(4*B*H*N^2*D, halved when causal), whole job over all ranks.
+  * value      device time: inputs already in HBM; per-step CUDA events on
+               the launching stream; the 129 MB L2 is flushed (a 256 MiB
+               write) between timed steps, outside the events.
+  * e2e        the same metric through the same C entry point with host
+               buffers: pinned host -> device copies of Q, K, V, the call,
+               and the device -> host copy of O and LSE, all inside the
+               timed region.
+  * roofline   tensor-bound: achieved = FLOPs per launch / mean launch time,
+               against the measured dense bf16 peak (fp16 has the same
+               nominal dense rate, so the ratio is 1).
+  * cpu_baseline  the FP64 CPU oracle, timed on a bounded row sample.
+N > 1 (torchrun): every rank runs the full workload on its own GPU (weak
+scaling, no collective on the data path); rank 0 prints the line with the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import fa_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "causal_fp16_b1h32n8192d128"
+# Pages' number for this exact workload and metric: PyTorch SDPA flash backend,
+# RTX 3060 Laptop (SM86), 25.854 ms at N=8192 ("CUDA FlashAttention: from online
+# softmax to the long-sequence IO limit", section 8, benchmark table).
+PAGE_MS = {"causal_fp16_b1h32n8192d128": 25.854, "causal_fp16_b1h32n4096d128": 6.573,
+           "causal_fp16_b1h32n2048d128": 1.704, "causal_fp16_b1h32n1024d128": 0.447,
+           "causal_fp16_b1h32n512d128": 0.149}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise MAX of a list of floats over all ranks (identity at world 1)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in values]
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_tflops(world, flops_per_rank, ms_per_step):
+    """Whole-job throughput: every rank did flops_per_rank in (at most) ms_per_step."""
+    return world * flops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("hbm_gbs", 6797.6)), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("exact_attention_22_gb300/csrc/fa_fwd.cu", "exact_attention_22_gb300/csrc/sm103_ptx.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    rec = d.get(workload_name)
+    if not rec or rec.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[2:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+_INPUT_CACHE = {}
+
+
+def _oracle_inputs(w, seed):
+    key = (w.name, seed)
+    if key not in _INPUT_CACHE:
+        q, k, v = fa_inputs.make_qkv(w, seed=seed)
+        _INPUT_CACHE.clear()
+        _INPUT_CACHE[key] = (fa_inputs.bits(q), fa_inputs.bits(k), fa_inputs.bits(v))
+    return _INPUT_CACHE[key]
+
+
+def cpu_oracle_sample(w, seconds=12.0, seed=0):
+    """Time the FP64 oracle on a bounded, fixed-order sample of the workload's
+    rows.  Returns (TFLOP/s, rows, seconds, threads, flops)."""
+    import numpy as np
+
+    from oracle import fa_ref
+
+    qb, kb, vb = _oracle_inputs(w, seed)
+    rng = np.random.default_rng(1234)
+    BH, N = w.B * w.H, w.N
+    order_bh = rng.integers(0, BH, 1 << 20)
+    order_row = rng.integers(0, N, 1 << 20)
+    threads = fa_ref.max_threads()
+    chunk = max(threads * 4, 64)
+    done, flops, t_total = 0, 0.0, 0.0
+    while (done == 0 or t_total < seconds) and done + chunk <= len(order_row):
+        bh = order_bh[done:done + chunk]
+        rows = order_row[done:done + chunk]
+        t0 = time.perf_counter()
+        fa_ref.naive_rows(qb, kb, vb, w.scale, w.causal, bh, rows, enc=fa_inputs.enc(w))
+        t_total += time.perf_counter() - t0
+        vis = (rows + 1) if w.causal else np.full(len(rows), N)
+        flops += float(np.sum(4.0 * vis * w.D))
+        done += chunk
+    # The FLOP model counts a causal row's half of the full square; the rows'
+    # exact visible-key count is used here, which is the same on average.
+    return flops / t_total / 1e12, done, t_total, threads, flops
+
+
+def run_reference(args, w):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    # The whole run is held to about two minutes of oracle time: each step is a
+    # row sample of seconds = 120 / (steps + warmup), at least one chunk of rows.
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, seconds=per_step)
+    vals, rows, secs, threads = [], 0, 0.0, 1
+    for _ in range(args.steps):
+        tf, r, s, threads, _ = cpu_oracle_sample(w, seconds=per_step)
+        vals.append(tf)
+        rows += r
+        secs += s
+    value = statistics.median(vals)
+    sample = "%d query rows drawn at random from all %d rows of the workload, %.1f s of FP64 oracle time" % (
+        rows, w.B * w.H * w.N, secs)
+    line = {
+        "impl": "reference", "metric": "attention fwd TFLOP/s (causal-adjusted)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / max(1, args.steps) * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1) inputs, see fa_inputs.py)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+                   "input_dtype": w.dtype},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_22_gb300 as fa
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    q_h, k_h, v_h = fa_inputs.make_qkv(w, seed=args.seed + rank)
+    q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream
+    dt = fa.FA_BF16 if w.dtype == "bf16" else fa.FA_FP16
+
+    def launch(qq, kk, vv, oo, ll):
+        st = fa.fa_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(), ll.data_ptr(), w.B, w.H, w.N,
+                       w.D, w.scale, int(w.causal), dt, handle)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch(q, k, v, o, lse)
+    torch.cuda.synchronize()
+    status = fa.fa_get_device_status(handle)
+    if status != fa.FA_OK:
+        raise fa.FaError(status, "warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            launch(q, k, v, o, lse)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    launches = args.steps
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    status = fa.fa_get_device_status(handle)
+    if status != fa.FA_OK:
+        raise fa.FaError(status, "timed region")
+
+    # End to end through host buffers: H2D of Q, K, V; the call; D2H of O, LSE.
+    qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
+    op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        q.copy_(qp, non_blocking=True); k.copy_(kp, non_blocking=True); v.copy_(vp, non_blocking=True)
+        launch(q, k, v, o, lse)
+        op.copy_(o, non_blocking=True); lp.copy_(lse, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        q.copy_(qp, non_blocking=True); k.copy_(kp, non_blocking=True); v.copy_(vp, non_blocking=True)
+        launch(q, k, v, o, lse)
+        op.copy_(o, non_blocking=True); lp.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], device=dev)
+    ms_per_step = total_ms / args.steps
+    value = job_tflops(world, w.flops, ms_per_step)
+    e2e_value = job_tflops(world, w.flops, e2e_ms)
+    peak, hbm, peak_kind = measured_peaks()
+    achieved = w.flops / (ms_per_step * 1e-3) / 1e12
+    clk = clocks.summary()
+
+    line = {
+        "metric": "attention fwd TFLOP/s (causal-adjusted)", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": (value / (w.flops / (PAGE_MS[w.name] * 1e-3) / 1e12)) if w.name in PAGE_MS else None,
+        "dtype": w.dtype, "data": "synthetic (seeded N(0,1) inputs, see fa_inputs.py)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+                   "scale": w.scale, "parallelism": "replica per GPU" if world > 1 else "single GPU",
+                   "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                   "ms_p50": statistics.median(step_ms), "ms_min": min(step_ms)},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                     "peak_kind": "%s dense bf16 (burst); fp16/bf16 nominal ratio 1" % peak_kind,
+                     "effective_GBps": w.io_bytes / (ms_per_step * 1e-3) / 1e9},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "kernel_source_sha": kernel_source_hash(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, rows, secs, threads, _ = cpu_oracle_sample(w, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "%d query rows drawn at random from the workload's %d rows, naive FP64 oracle, %.1f s"
+                      % (rows, w.B * w.H * w.N, secs)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(fa_inputs.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = fa_inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

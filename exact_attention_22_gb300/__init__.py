@@ -1,0 +1,9 @@
+"""Exact attention forward pass on GB300 (sm_103a).
+
+The compute path is the CUDA library ``libfa.so`` (built from ``csrc/``); this
+package only marshals arguments to its C ABI (``include/fa.h``).  There is no
+CPU or PyTorch fallback: if the library is missing, importing the binding
+raises.
+"""
+from .binding import (FA_BF16, FA_FP16, FA_OK, FaError, STATUS_NAMES, attention, fa_fwd,  # noqa: F401
+                      fa_get_device_status, fa_status_string, library_path, load_library)

@@ -1,0 +1,101 @@
+"""ctypes binding of libfa.so: the same entry points as include/fa.h.
+
+``fa_fwd`` / ``fa_get_device_status`` / ``fa_status_string`` take plain
+integers (device pointers, sizes, a stream handle) exactly like the C ABI.
+``attention`` is a convenience wrapper for torch CUDA tensors: it only checks
+shapes, allocates the outputs with torch and passes pointers through.  Every
+step of the computation runs in the CUDA library.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libfa.so")
+
+FA_FP16, FA_BF16 = 0, 1
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
+                4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__("%s returned %s" % (where, STATUS_NAMES.get(status, status)))
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libfa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("libfa.so is not built (run exact_attention_22_gb300.build.build() or "
+                               "__graft_entry__.build()); there is no fallback path")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, I, vp]
+        lib.fa_fwd.restype = I
+        lib.fa_get_device_status.argtypes = [vp]
+        lib.fa_get_device_status.restype = I
+        lib.fa_status_string.argtypes = [I]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, D: int, scale: float,
+           causal: int, dtype: int, stream: int) -> int:
+    """Direct call of the C entry point; returns its status code."""
+    return int(load_library().fa_fwd(q, k, v, o, lse, B, H, N, D, float(scale), int(causal), int(dtype),
+                                     stream))
+
+
+def fa_get_device_status(stream: int) -> int:
+    return int(load_library().fa_get_device_status(stream))
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+    """O, LSE = attention(Q, K, V) for contiguous [B,H,N,D] fp16/bf16 CUDA tensors.
+
+    Outputs are allocated with torch when not given.  Raises FaError on a
+    non-OK status.  Asynchronous on ``stream`` (default: torch's current stream).
+    """
+    import torch
+
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, float16 or bfloat16")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [B, H, N, D]")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D, scale,
+                int(bool(causal)), FA_BF16 if q.dtype == torch.bfloat16 else FA_FP16, handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+    return out, lse

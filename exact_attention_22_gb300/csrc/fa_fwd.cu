@@ -1,0 +1,723 @@
+// fa_fwd.cu -- exact attention forward pass for sm_103a (GB300), behind the
+// C ABI declared in include/fa.h.
+//
+// What is computed follows "CUDA FlashAttention: from online softmax to the
+// long-sequence IO limit" (sections 4-6) and "Why FlashAttention does not
+// need to store the attention matrix" (sections 3.2, 4.1, 4.5): per query
+// row, a running max m, a running sum l and an unnormalised output O are
+// carried across key/value tiles; a new tile's scores are masked (causal
+// diagonal, ragged tail) before the tile max, O and l are rescaled by
+// 2^(m_old - m_new) before the tile's P V is added, and the row ends with
+// O / l and LSE = m + log l.  Tiles entirely above the causal diagonal are
+// never visited.
+//
+// How it is computed is this file's own design for Blackwell:
+//   * one CTA = 256 query rows of one (b, h) = two 128-row Q tiles that share
+//     every K/V tile;
+//   * TMA loads Q once and streams K_j, V_j through a shared-memory ring
+//     (128-byte swizzle, mbarrier full/empty pairs);
+//   * one thread issues tcgen05 UMMAs: S_t = Q_t K_j^T into tensor memory
+//     (TMEM), and O_t += P_t V_j with P_t read back from TMEM, where it
+//     overwrites the first half of S_t;
+//   * a softmax warpgroup per Q tile owns one row per thread: it loads the S
+//     row from TMEM, masks, takes the max, exponentiates in base 2 and writes
+//     P_t (16-bit) back to TMEM;
+//   * a correction warpgroup rescales O_t in TMEM when a row's reference max
+//     moves by more than 2^8 (the reference may lag the true max: the
+//     invariant O = sum e^(s - m_ref) v, l = sum e^(s - m_ref) holds for any
+//     m_ref used consistently, so the result is unchanged), and finally
+//     writes O / l through a TMA store and LSE with plain stores;
+//   * the two Q tiles ping-pong: while one softmax warpgroup exponentiates,
+//     the tensor core works on the other tile.
+// Every mbarrier wait is bounded in time; a wait that gives up records a
+// status bit, makes the other roles stop, drains in-flight copies and MMAs,
+// frees TMEM and returns.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "sm103_ptx.cuh"
+
+namespace fa103 {
+
+// Status word of this library on each device: bits of the roles that gave up.
+__device__ unsigned int g_fa_status;
+
+enum : unsigned {
+    ST_PRODUCER = 1u,
+    ST_MMA = 2u,
+    ST_SOFTMAX = 4u,
+    ST_CORRECTION = 8u,
+    ST_DRAIN = 16u,
+};
+
+constexpr int kTileM = 128;     // query rows of one Q tile (UMMA M)
+constexpr int kTileN = 128;     // keys of one K/V tile (UMMA N of S, K of P V)
+constexpr int kNumQ = 2;        // Q tiles per CTA
+constexpr int kRowsPerCta = kTileM * kNumQ;
+constexpr int kThreads = 128 * (2 + kNumQ);   // producer/MMA WG, softmax WGs, correction WG
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;   // 1 s per wait
+constexpr float kLazyRescale = 8.0f;          // log2 units: rescale only when the max grows > 2^8
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct Cfg {
+    static constexpr int kTileBytes = kTileM * D * 2;   // one 128-row tile of Q, K, V or O
+    static constexpr int kBoxes = D / 64;               // 64-element (128-byte) swizzle boxes along D
+    static constexpr int kBoxBytes = kTileM * 128;
+    static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring slots
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kNumQ * kTileBytes;
+    static constexpr int kSmemBytes = kOffKV + kStages * kTileBytes + 1024;   // + 1 KB alignment slack
+    // TMEM column map: S_t (128 fp32 columns, P_t aliases its first 64), O_t (D columns)
+    __host__ __device__ static constexpr uint32_t tm_s(int t) { return 128u * t; }
+    __host__ __device__ static constexpr uint32_t tm_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+};
+
+struct __align__(8) SharedState {
+    uint64_t q_full;
+    uint64_t kv_full[8];
+    uint64_t kv_empty[8];
+    uint64_t s_full[kNumQ];        // MMA -> softmax: S_t of the current tile is in TMEM
+    uint64_t p_full[kNumQ];        // softmax -> MMA: P_t written to TMEM
+    uint64_t alpha_ready[kNumQ];   // softmax -> correction: per-row rescale factors published
+    uint64_t o_ready[kNumQ];       // correction -> MMA: O_t rescaled, P_t V may accumulate
+    uint64_t pv_done[kNumQ];       // MMA -> correction: O_t += P_t V_j complete
+    uint64_t stats_ready[kNumQ];   // softmax -> epilogue: final m, l of every row
+    uint64_t drain;
+    float alpha[kNumQ][kTileM];
+    float row_m[kNumQ][kTileM];
+    float row_l[kNumQ][kTileM];    // sum of the rounded P used by P V: normalises O
+    float row_ls[kNumQ][kTileM];   // sum of the fp32 p: the log-sum-exp
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct Params {
+    float* lse;
+    int N;
+    int BH;
+    int n_qblocks;       // ceil(N / 256)
+    float scale_log2;    // scale * log2(e)
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+    }
+}
+
+__device__ __forceinline__ void give_up(SharedState& sh, unsigned code) {
+    atomicOr(&g_fa_status, code);
+    *reinterpret_cast<volatile int*>(&sh.abort_flag) = 1;
+}
+
+template <int N_>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N_));
+}
+template <int N_>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N_));
+}
+
+// 128 consecutive TMEM columns of this thread's lane, one wait for all four loads.
+__device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, float (&s)[128]) {
+    uint32_t(&r)[128] = reinterpret_cast<uint32_t(&)[128]>(s);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
+        "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,"
+        "%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
+        "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%129];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]),
+          "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+          "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+          "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+          "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]),
+          "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]),
+          "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]),
+          "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]),
+          "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]),
+          "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]),
+          "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]),
+          "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]),
+          "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]),
+          "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+        : "r"(taddr), "r"(taddr + 64)
+        : "memory");
+}
+
+// ------------------------------------------------------------------ roles
+
+template <int D>
+__device__ void run_producer(SharedState& sh, uint8_t* tiles, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                             const CUtensorMap* tm_v, int q0, int bh, const int (&nkv)[kNumQ], int n_all) {
+    using C = Cfg<D>;
+    volatile int* abort_flag = &sh.abort_flag;
+    prefetch_tmap(tm_q);
+    prefetch_tmap(tm_k);
+    prefetch_tmap(tm_v);
+    const uint64_t pol_keep = l2_policy_evict_last();    // K, V: re-read by the head's other CTAs
+    const uint64_t pol_once = l2_policy_evict_first();   // Q: read once
+
+    int nq_active = 0;
+    for (int t = 0; t < kNumQ; ++t) nq_active += nkv[t] > 0;
+    mbar_arrive_expect_tx(&sh.q_full, nq_active * C::kTileBytes);
+    for (int t = 0; t < kNumQ; ++t) {
+        if (nkv[t] == 0) continue;
+        for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d_hint(tiles + C::kOffQ + t * C::kTileBytes + b * C::kBoxBytes, tm_q, &sh.q_full, 64 * b,
+                             q0 + kTileM * t, bh, pol_once);
+    }
+
+    int last_item[C::kStages];
+    for (int s = 0; s < C::kStages; ++s) last_item[s] = -1;
+    int item = 0;
+    bool ok = true;
+    for (int j = 0; j < n_all && ok; ++j) {
+        for (int kind = 0; kind < 2; ++kind, ++item) {   // K_j, then V_j
+            const int slot = item % C::kStages;
+            const uint32_t phase = (item / C::kStages) & 1;
+            if (!wait_bar(&sh.kv_empty[slot], phase ^ 1, abort_flag)) {
+                give_up(sh, ST_PRODUCER);
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(&sh.kv_full[slot], C::kTileBytes);
+            const CUtensorMap* map = kind ? tm_v : tm_k;
+            for (int b = 0; b < C::kBoxes; ++b)
+                tma_load_3d_hint(tiles + C::kOffKV + slot * C::kTileBytes + b * C::kBoxBytes, map,
+                                 &sh.kv_full[slot], 64 * b, j * kTileN, bh, pol_keep);
+            last_item[slot] = item;
+        }
+    }
+    if (!ok) {
+        // Let every copy already issued land before the CTA's shared memory goes away.
+        volatile int never = 0;
+        wait_bar(&sh.q_full, 0, &never);
+        for (int s = 0; s < C::kStages; ++s)
+            if (last_item[s] >= 0) wait_bar(&sh.kv_full[s], (last_item[s] / C::kStages) & 1, &never);
+    }
+}
+
+template <int D, bool BF16>
+__device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const int (&nkv)[kNumQ], int n_all) {
+    using C = Cfg<D>;
+    volatile int* abort_flag = &sh.abort_flag;
+    constexpr uint32_t kIdS = idesc_f16(BF16, kTileM, kTileN, false);
+    constexpr uint32_t kIdO = idesc_f16(BF16, kTileM, D, true);
+    const uint32_t sq = smem_u32(tiles + C::kOffQ);
+    const uint32_t skv = smem_u32(tiles + C::kOffKV);
+
+    auto issue_s = [&](int t, int slot) {
+        const uint32_t qa = sq + t * C::kTileBytes, kb = skv + slot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+            umma_ss(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdS,
+                    kk > 0);
+        }
+    };
+    auto issue_pv = [&](int t, int slot, bool first) {
+        const uint32_t vb = skv + slot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+            umma_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + kk * 8, sdesc_sw128(vb + kk * 2048, C::kBoxBytes, 1024),
+                    kIdO, !(first && kk == 0));
+    };
+    auto ring_wait = [&](int item) -> bool {
+        return wait_bar(&sh.kv_full[item % C::kStages], (item / C::kStages) & 1, abort_flag);
+    };
+
+    bool ok = wait_bar(&sh.q_full, 0, abort_flag);
+    int item = 0;
+    if (ok) ok = ring_wait(item);   // K_0
+    if (ok) {
+        tc_fence_after();
+        const int slot = item % C::kStages;
+        for (int t = 0; t < kNumQ; ++t)
+            if (nkv[t] > 0) {
+                issue_s(t, slot);
+                umma_commit(&sh.s_full[t]);
+            }
+        umma_commit(&sh.kv_empty[slot]);
+        ++item;
+    }
+    for (int j = 0; j < n_all && ok; ++j) {
+        const int item_v = item++;
+        if (!ring_wait(item_v)) { ok = false; break; }
+        const int slot_v = item_v % C::kStages;
+        const bool has_next = j + 1 < n_all;
+        const int item_k = has_next ? item++ : -1;
+        bool k_ready = false;
+        for (int t = 0; t < kNumQ && ok; ++t) {
+            if (j >= nkv[t]) continue;
+            if (!wait_bar(&sh.p_full[t], j & 1, abort_flag) || !wait_bar(&sh.o_ready[t], j & 1, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            issue_pv(t, slot_v, j == 0);
+            umma_commit(&sh.pv_done[t]);
+            if (j + 1 < nkv[t]) {
+                if (!k_ready) {
+                    if (!ring_wait(item_k)) { ok = false; break; }
+                    tc_fence_after();
+                    k_ready = true;
+                }
+                issue_s(t, item_k % C::kStages);
+                umma_commit(&sh.s_full[t]);
+            }
+        }
+        if (!ok) break;
+        umma_commit(&sh.kv_empty[slot_v]);
+        if (has_next) {
+            if (!k_ready && !ring_wait(item_k)) { ok = false; break; }
+            umma_commit(&sh.kv_empty[item_k % C::kStages]);
+        }
+    }
+    if (!ok) give_up(sh, ST_MMA);
+    // Nothing of ours may still be in flight when the CTA retires.
+    umma_commit(&sh.drain);
+    volatile int never = 0;
+    if (!wait_bar(&sh.drain, 0, &never)) atomicOr(&g_fa_status, ST_DRAIN);
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, int q0, int N, float scale_log2, int nkv_t) {
+    volatile int* abort_flag = &sh.abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = threadIdx.x - 128 * (1 + t);               // row of this thread in Q tile t
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t ts = tmem + lane_addr + Cfg<D>::tm_s(t);
+    const int qi = q0 + kTileM * t + r;                       // global query index
+
+    float m_ref = -INFINITY;   // reference max, log2 units of the scaled score
+    float l = 0.f;             // running sum of the 16-bit-rounded P actually used by P V
+    float ls = 0.f;            // running sum of the unrounded p, for the log-sum-exp
+    for (int j = 0; j < nkv_t; ++j) {
+        bool ok = wait_bar(&sh.s_full[t], j & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            give_up(sh, ST_SOFTMAX);
+            break;
+        }
+        tc_fence_after();
+        float s[kTileN];
+        tmem_ld128_wait(ts, s);
+
+        // Scale into log2 units first and take the max of those rounded values,
+        // so the row's largest element maps to exactly 2^0 however large the
+        // scores are (subtracting a separately rounded max inside one fma can
+        // leave an error of many units when |s| is huge).
+        const int k0 = j * kTileN;
+        const bool need_mask = (CAUSAL && j == nkv_t - 1) || (k0 + kTileN > N);
+#pragma unroll
+        for (int c = 0; c < kTileN; ++c) s[c] *= scale_log2;
+        if (need_mask) {
+#pragma unroll
+            for (int c = 0; c < kTileN; ++c) {
+                const int key = k0 + c;
+                if (key >= N || (CAUSAL && key > qi)) s[c] = -INFINITY;
+            }
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < kTileN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+        const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_new = fmaxf(m_ref, m_tile);
+        float alpha = 1.f;
+        if (m_ref == -INFINITY) {
+            alpha = 0.f;            // nothing accumulated yet
+            m_ref = m_new;
+        } else if (m_new > m_ref + kLazyRescale) {
+            alpha = ex2_approx(m_ref - m_new);
+            m_ref = m_new;
+        }
+        sh.alpha[t][r] = alpha;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.alpha_ready[t]);
+
+        const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
+        float lt[4] = {0.f, 0.f, 0.f, 0.f};
+        float lx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float p0 = ex2_approx(s[64 * h + 2 * i] - msub);
+                const float p1 = ex2_approx(s[64 * h + 2 * i + 1] - msub);
+                uint32_t w;
+                float r0, r1;
+                if constexpr (BF16) {
+                    w = pack_bf16x2(p0, p1);
+                    r0 = __uint_as_float(w << 16);
+                    r1 = __uint_as_float(w & 0xffff0000u);
+                } else {
+                    w = pack_f16x2(p0, p1);
+                    r0 = __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+                    r1 = __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+                }
+                pk[i] = w;
+                lt[i & 3] += r0 + r1;
+                lx[i & 3] += p0 + p1;
+            }
+            tmem_st32(ts + 32 * h, pk);
+        }
+        l = l * alpha + ((lt[0] + lt[1]) + (lt[2] + lt[3]));
+        ls = ls * alpha + ((lx[0] + lx[1]) + (lx[2] + lx[3]));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.p_full[t]);
+    }
+    sh.row_m[t][r] = m_ref;
+    sh.row_l[t][r] = l;
+    sh.row_ls[t][r] = ls;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.stats_ready[t]);
+}
+
+// Named barrier over the correction warpgroup whose result is the OR of `pred`.
+__device__ __forceinline__ bool wg_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
+}
+
+template <int D, bool BF16>
+__device__ void run_correction(SharedState& sh, uint8_t* tiles, uint32_t tmem, const CUtensorMap* tm_o,
+                               const Params& p, int q0, int bh, const int (&nkv)[kNumQ], int n_all) {
+    using C = Cfg<D>;
+    volatile int* abort_flag = &sh.abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = threadIdx.x - 128 * (1 + kNumQ);
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+
+    bool ok = true;
+    for (int j = 0; j < n_all && ok; ++j) {
+        for (int t = 0; t < kNumQ; ++t) {
+            if (j >= nkv[t]) continue;
+            ok = __all_sync(0xffffffffu, wait_bar(&sh.alpha_ready[t], j & 1, abort_flag));
+            if (!ok) break;
+            if (j > 0) {
+                const float a = sh.alpha[t][r];
+                if (__any_sync(0xffffffffu, a != 1.f)) {
+                    // O_t holds P V of tiles 0..j-1; its last update finished before S_t(j) did.
+                    ok = __all_sync(0xffffffffu, wait_bar(&sh.pv_done[t], (j - 1) & 1, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t to = tmem + lane_addr + C::tm_o(t);
+#pragma unroll
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld32_wait(to + c, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+                        tmem_st32(to + c, v);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.o_ready[t]);
+        }
+    }
+    if (!ok) give_up(sh, ST_CORRECTION);
+
+    // Epilogue: O / l -> 16-bit -> swizzled staging (the Q tile's buffer) -> TMA store; LSE.
+    bool stored = false;
+    for (int t = 0; t < kNumQ; ++t) {
+        if (nkv[t] == 0) continue;
+        bool good = ok && __all_sync(0xffffffffu, wait_bar(&sh.stats_ready[t], 0, abort_flag));
+        good = good && __all_sync(0xffffffffu, wait_bar(&sh.pv_done[t], (nkv[t] - 1) & 1, abort_flag));
+        uint8_t* stage = tiles + C::kOffQ + t * C::kTileBytes;
+        const int r0 = q0 + kTileM * t;
+        if (good) {
+            tc_fence_after();
+            const float m = sh.row_m[t][r], l = sh.row_l[t][r], ls = sh.row_ls[t][r];
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const uint32_t to = tmem + lane_addr + C::tm_o(t);
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t v[32];
+                tmem_ld32_wait(to + c, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float x0 = __uint_as_float(v[2 * i]) * inv, x1 = __uint_as_float(v[2 * i + 1]) * inv;
+                    pk[i] = BF16 ? pack_bf16x2(x0, x1) : pack_f16x2(x0, x1);
+                }
+                const int box = c / 64;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int chunk = (c % 64) / 8 + q;                     // 16-byte chunk within the 128-B row
+                    uint8_t* dst = stage + box * C::kBoxBytes + r * 128 + ((chunk ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            const int row = r0 + r;
+            if (row < p.N)
+                p.lse[static_cast<size_t>(bh) * p.N + row] =
+                    ls > 0.f ? (m + log2f(ls)) * 0.69314718055994531f : -INFINITY;
+            fence_proxy_async_smem();
+        }
+        const bool any_bad = wg_any(!good);
+        if (!any_bad && r == 0) {
+            for (int b = 0; b < C::kBoxes; ++b) tma_store_3d(tm_o, stage + b * C::kBoxBytes, 64 * b, r0, bh);
+            bulk_commit();
+            stored = true;
+        }
+        if (any_bad) ok = false;
+    }
+    if (stored) bulk_wait_all();
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const Params p) {
+    extern __shared__ uint8_t dyn_smem[];
+    __shared__ SharedState sh;
+    uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
+
+    // Heaviest query blocks first (causal work grows with the block index).
+    const int qb = p.n_qblocks - 1 - static_cast<int>(blockIdx.x / p.BH);
+    const int bh = static_cast<int>(blockIdx.x % p.BH);
+    const int q0 = qb * kRowsPerCta;
+    int nkv[kNumQ];
+    int n_all = 0;
+#pragma unroll
+    for (int t = 0; t < kNumQ; ++t) {
+        const int r0 = q0 + kTileM * t;
+        if (r0 >= p.N)
+            nkv[t] = 0;
+        else if (CAUSAL)
+            nkv[t] = min(r0 + kTileM - 1, p.N - 1) / kTileN + 1;
+        else
+            nkv[t] = (p.N + kTileN - 1) / kTileN;
+        n_all = max(n_all, nkv[t]);
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sh.q_full, 1);
+        for (int s = 0; s < Cfg<D>::kStages; ++s) {
+            mbar_init(&sh.kv_full[s], 1);
+            mbar_init(&sh.kv_empty[s], 1);
+        }
+        for (int t = 0; t < kNumQ; ++t) {
+            mbar_init(&sh.s_full[t], 1);
+            mbar_init(&sh.p_full[t], 4);
+            mbar_init(&sh.alpha_ready[t], 4);
+            mbar_init(&sh.o_ready[t], 4);
+            mbar_init(&sh.pv_done[t], 1);
+            mbar_init(&sh.stats_ready[t], 4);
+        }
+        mbar_init(&sh.drain, 1);
+        sh.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sh.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (wg == 0) {
+        setmaxnreg_dec<48>();
+        if (warp == 0 && lane == 0)
+            run_producer<D>(sh, tiles, &tm_q, &tm_k, &tm_v, q0, bh, nkv, n_all);
+        else if (warp == 1 && lane == 0)
+            run_mma<D, BF16>(sh, tiles, tmem, nkv, n_all);
+        __syncwarp();
+    } else if (wg <= kNumQ) {
+        setmaxnreg_inc<192>();
+        const int t = wg - 1;
+        if (nkv[t] > 0) run_softmax<D, BF16, CAUSAL>(sh, tmem, t, q0, p.N, p.scale_log2, nkv[t]);
+    } else {
+        setmaxnreg_dec<80>();
+        run_correction<D, BF16>(sh, tiles, tmem, &tm_o, p, q0, bh, nkv, n_all);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+// [B*H, N, D] view, 128-row x 64-column boxes with the 128-byte swizzle.
+static bool make_tile_map(CUtensorMap* map, const void* base, int dtype, int D, int N, int BH) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTileM), 1};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void*>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                          const Params& p, cudaStream_t stream) {
+    auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
+    static std::atomic<uint64_t> configured{0};   // one bit per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (!bit || !(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    const unsigned grid = static_cast<unsigned>(p.n_qblocks) * static_cast<unsigned>(p.BH);
+    kern<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(q, k, v, o, p);
+    return cudaGetLastError();
+}
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+}  // namespace fa103
+
+using namespace fa103;
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+                      float scale, int causal, int dtype, cudaStream_t stream) {
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    const void* ptrs[5] = {q, k, v, o, lse};
+    for (const void* ptr : ptrs)
+        if (ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return FA_ERR_MISALIGNED;
+    const uint64_t BH = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
+    const uint64_t elems = BH * static_cast<uint64_t>(N) * static_cast<uint64_t>(D);
+    if (BH > 0x7fffffffull || elems >= (uint64_t(1) << 40)) return FA_ERR_INVALID_ARG;
+    const uint64_t n_qblocks = (static_cast<uint64_t>(N) + kRowsPerCta - 1) / kRowsPerCta;
+    if (n_qblocks * BH > 0x7fffffffull) return FA_ERR_INVALID_ARG;
+    const size_t tbytes = static_cast<size_t>(elems) * 2, lbytes = static_cast<size_t>(BH) * N * sizeof(float);
+    const void* ins[3] = {q, k, v};
+    for (const void* in : ins)
+        if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes)) return FA_ERR_INVALID_ARG;
+    if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
+
+    CUtensorMap mq, mk, mv, mo;
+    const int bh = static_cast<int>(BH);
+    if (!make_tile_map(&mq, q, dtype, D, N, bh) || !make_tile_map(&mk, k, dtype, D, N, bh) ||
+        !make_tile_map(&mv, v, dtype, D, N, bh) || !make_tile_map(&mo, o, dtype, D, N, bh))
+        return FA_ERR_CUDA;
+
+    Params p;
+    p.lse = lse;
+    p.N = N;
+    p.BH = bh;
+    p.n_qblocks = static_cast<int>(n_qblocks);
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+    cudaError_t e;
+    const bool bf = dtype == FA_BF16;
+#define FA_LAUNCH(DD, BB, CC) e = launch<DD, BB, CC>(mq, mk, mv, mo, p, stream)
+    if (D == 64) {
+        if (bf) { if (causal) FA_LAUNCH(64, true, true); else FA_LAUNCH(64, true, false); }
+        else    { if (causal) FA_LAUNCH(64, false, true); else FA_LAUNCH(64, false, false); }
+    } else {
+        if (bf) { if (causal) FA_LAUNCH(128, true, true); else FA_LAUNCH(128, true, false); }
+        else    { if (causal) FA_LAUNCH(128, false, true); else FA_LAUNCH(128, false, false); }
+    }
+#undef FA_LAUNCH
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" int fa_get_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof v) != cudaSuccess) return FA_ERR_CUDA;
+    if (v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof zero) != cudaSuccess) return FA_ERR_CUDA;
+        return FA_ERR_TIMEOUT;
+    }
+    return FA_OK;
+}
+
+extern "C" const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}

@@ -1,0 +1,79 @@
+/*
+ * fa.h -- C ABI of the exact attention forward pass on sm_103a (GB300).
+ *
+ * The operation ("CUDA FlashAttention: from online softmax to the
+ * long-sequence IO limit", sections 1 and 4; "Why FlashAttention does not
+ * need to store the attention matrix", sections 3.2 and 4.1):
+ *
+ *     O   = softmax(scale * Q K^T + M) V
+ *     LSE = log(sum_j exp(scale * q_i . k_j + M_ij))          (natural log)
+ *
+ * with M_ij = -inf for j > i when `causal` is 1 and M = 0 otherwise.  The
+ * N x N score and probability matrices never reach device memory: each
+ * 128-row query block keeps an FP32 running max m, running sum l and an
+ * unnormalised output across the key/value blocks, rescaled by
+ * exp(m_old - m_new), and writes O = O / l plus LSE = m + log(l) at the end.
+ *
+ * Layout: Q, K, V and O are [B, H, N, D] row-major and contiguous, all of the
+ * same 16-bit type; LSE is [B, H, N] fp32.  Every pointer passed to fa_fwd is
+ * a DEVICE pointer owned by the caller; the library allocates nothing per
+ * call and keeps no pointer after it returns.  O and LSE must not overlap Q,
+ * K or V (or each other).
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* bad size, flag, scale, or overlapping outputs  */
+    FA_ERR_UNSUPPORTED = 2,   /* head dimension other than 64 or 128           */
+    FA_ERR_MISALIGNED = 3,    /* null pointer or not 16-byte aligned           */
+    FA_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed          */
+    FA_ERR_TIMEOUT = 5        /* a bounded in-kernel wait gave up (see below)  */
+} fa_status;
+
+/*
+ * fa_fwd -- launch the forward pass on `stream`; returns without waiting.
+ *
+ *   q, k, v    [B,H,N,D] input, type `dtype`                (device, read)
+ *   o          [B,H,N,D] output, type `dtype`                (device, written)
+ *   lse        [B,H,N] fp32 natural-log log-sum-exp          (device, written)
+ *   B, H, N    batch, heads, sequence length; each >= 1, B*H*N*D < 2^40
+ *   D          head dimension: 64 or 128, else FA_ERR_UNSUPPORTED
+ *   scale      softmax scale applied to Q K^T (usually 1/sqrt(D)); finite, > 0
+ *   causal     0: no mask; 1: the square lower-triangular mask (key j <= query i)
+ *   dtype      FA_FP16 or FA_BF16
+ *   stream     CUDA stream (0 = legacy default stream)
+ *
+ * Returns FA_OK once the kernel is queued.  Argument errors are reported
+ * before anything is launched and leave o / lse untouched.  N need not be a
+ * multiple of any tile size.  Results are deterministic for fixed inputs.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int D, float scale, int causal, int dtype,
+           cudaStream_t stream);
+
+/*
+ * fa_get_device_status -- synchronise `stream`, then report whether any
+ * kernel of this library on the current device gave up on a bounded wait
+ * since the last call (FA_ERR_TIMEOUT; the outputs of that launch are
+ * undefined), or whether the stream holds a CUDA error (FA_ERR_CUDA).
+ * Reading the status clears it.
+ */
+int fa_get_device_status(cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* fa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FA_GB300_FA_H */

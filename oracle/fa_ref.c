@@ -41,11 +41,32 @@ static double decode_bfloat16(uint16_t b)
     return (double)x;
 }
 
+/* Every 16-bit pattern decoded once by the functions above; the inner loops
+ * then look values up instead of decoding them again. */
+static double g_dec_f16[65536], g_dec_bf16[65536];
+static int g_dec_ready = 0;
+
+static void build_decode_tables(void)
+{
+    if (g_dec_ready) return;
+#pragma omp critical(fa_ref_decode_tables)
+    {
+        if (!g_dec_ready) {
+            for (uint32_t h = 0; h < 65536u; ++h) {
+                g_dec_f16[h] = decode_binary16((uint16_t)h);
+                g_dec_bf16[h] = decode_bfloat16((uint16_t)h);
+            }
+#pragma omp flush
+            g_dec_ready = 1;
+        }
+    }
+}
+
 static double load(const void* p, int enc, size_t idx)
 {
     switch (enc) {
-    case FA_REF_ENC_F16:  return decode_binary16(((const uint16_t*)p)[idx]);
-    case FA_REF_ENC_BF16: return decode_bfloat16(((const uint16_t*)p)[idx]);
+    case FA_REF_ENC_F16:  return g_dec_f16[((const uint16_t*)p)[idx]];
+    case FA_REF_ENC_BF16: return g_dec_bf16[((const uint16_t*)p)[idx]];
     default:              return ((const double*)p)[idx];
     }
 }
@@ -56,6 +77,7 @@ static int bad_args(const void* q, const void* k, const void* v, int enc,
     if (!q || !k || !v) return 1;
     if (B < 1 || H < 1 || N < 1 || D < 1) return 1;
     if (enc != FA_REF_ENC_F64 && enc != FA_REF_ENC_F16 && enc != FA_REF_ENC_BF16) return 1;
+    build_decode_tables();
     return 0;
 }
 

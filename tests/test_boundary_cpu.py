@@ -1,0 +1,76 @@
+"""The C ABI without a GPU: the library builds and loads, exports what
+include/fa.h declares, and rejects bad arguments before touching CUDA."""
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+import exact_attention_22_gb300 as fa
+from exact_attention_22_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load_library()
+
+
+def _declared():
+    names = set()
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if hdr.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", hdr)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(fa_\w+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert {"fa_fwd", "fa_get_device_status", "fa_status_string"} <= declared
+    out = subprocess.check_output(["nm", "-D", "--defined-only", fa.library_path()], text=True)
+    exported = set(re.findall(r"\bT (fa_\w+)", out))
+    assert declared <= exported, declared - exported
+
+
+def test_status_strings(lib):
+    for code, name in fa.STATUS_NAMES.items():
+        assert fa.fa_status_string(code) == name
+    assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+# Fake but 16-byte-aligned, non-overlapping "device" addresses: every call
+# below must fail validation before any CUDA call is made.
+GOOD = dict(q=1 << 20, k=2 << 20, v=3 << 20, o=4 << 20, lse=5 << 20, B=1, H=2, N=256, D=64,
+            scale=0.125, causal=0, dtype=0, stream=0)
+
+
+def _call(**kw):
+    a = dict(GOOD, **kw)
+    return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"], a["scale"],
+                     a["causal"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), 2), (dict(D=32), 2), (dict(D=256), 2),
+    (dict(B=0), 1), (dict(H=-1), 1), (dict(N=0), 1),
+    (dict(causal=2), 1), (dict(dtype=2), 1),
+    (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=math.inf), 1), (dict(scale=math.nan), 1),
+    (dict(q=0), 3), (dict(o=0), 3), (dict(lse=0), 3), (dict(k=(2 << 20) + 8), 3), (dict(v=(3 << 20) + 2), 3),
+    (dict(o=(1 << 20) + 4096), 1),           # output overlaps q
+    (dict(lse=(4 << 20) + 64), 1),           # lse overlaps o
+    (dict(B=1 << 16, H=1 << 16), 1),         # B*H does not fit the grid
+])
+def test_argument_errors(lib, kw, status):
+    assert _call(**kw) == status
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        fa.attention(x, x, x)

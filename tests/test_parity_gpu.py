@@ -1,0 +1,171 @@
+"""Parity of the CUDA path (through the C ABI) with the FP64 oracle.
+
+Small shapes are compared element by element; the full-size workloads, run in
+the same launch configuration the bench uses, are compared on sampled rows
+the oracle evaluates one by one.  Tolerances (against the FP64 oracle on the
+same 16-bit-rounded inputs): max |dO| <= 2e-3 for fp16 outputs, <= 1e-2 for
+bf16 outputs, max |dLSE| <= 1e-3.  For the peaky bf16 workload (scores with
+a standard deviation of 9, not N(0,1) inputs) the bf16 rounding of O alone
+can exceed 1e-2 where |O| >= 4, so each element there may also use half a
+bf16 ulp of the exact value on top of 1e-2.
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_22_gb300 as fa
+import fa_inputs
+from oracle import fa_ref
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = {"fp16": 2e-3, "bf16": 1e-2}
+TOL_LSE = 1e-3
+
+
+def _run(q, k, v, causal, scale, stream=None):
+    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, stream=stream)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def _bf16_half_ulp(x):
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return 0.5 * 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+def _check(o, lse, o_ref, lse_ref, dtype, peaky=False, what=""):
+    o = o.float().cpu().numpy().reshape(o_ref.shape)
+    lse = lse.cpu().numpy().reshape(lse_ref.shape)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), what
+    err = np.abs(o - o_ref)
+    tol = TOL_O[dtype] + (_bf16_half_ulp(o_ref) if peaky else 0.0)
+    bad = err > tol
+    assert not bad.any(), "%s: %d elements over tolerance, max|dO|=%.3e" % (what, bad.sum(), err.max())
+    el = np.abs(lse - lse_ref).max()
+    assert el <= TOL_LSE, "%s: max|dLSE|=%.3e" % (what, el)
+    return float(err.max()), float(el)
+
+
+def _oracle_full(q, k, v, causal, scale):
+    e = fa_inputs.enc(q.dtype)
+    return fa_ref.naive(fa_inputs.bits(q), fa_inputs.bits(k), fa_inputs.bits(v), scale, causal, enc=e)
+
+
+SMALL_N = [1, 2, 3, 17, 127, 128, 129, 255, 256, 257, 300, 511, 1000]
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("N", SMALL_N)
+def test_small_shapes_elementwise(N, D, causal, dtype):
+    w = fa_inputs.Workload("small", 1, 2, N, D, causal, dtype)
+    q, k, v = fa_inputs.make_qkv(w, seed=N * 7 + D)
+    o, lse = _run(q, k, v, causal, w.scale)
+    o_ref, lse_ref = _oracle_full(q, k, v, causal, w.scale)
+    _check(o, lse, o_ref, lse_ref, dtype, what="N=%d D=%d causal=%d %s" % (N, D, causal, dtype))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_batch_and_head_indexing(causal):
+    w = fa_inputs.Workload("bh", 2, 3, 333, 128, causal, "bf16")
+    q, k, v = fa_inputs.make_qkv(w, seed=5)
+    o, lse = _run(q, k, v, causal, w.scale)
+    o_ref, lse_ref = _oracle_full(q, k, v, causal, w.scale)
+    _check(o, lse, o_ref, lse_ref, "bf16", what="B2 H3 N333")
+
+
+def test_tiny_workload_elementwise():
+    w = fa_inputs.WORKLOADS["tiny_fp16_b1h2n256d64"]
+    q, k, v = fa_inputs.make_qkv(w, seed=0)
+    o, lse = _run(q, k, v, w.causal, w.scale)
+    o_ref, lse_ref = _oracle_full(q, k, v, w.causal, w.scale)
+    _check(o, lse, o_ref, lse_ref, w.dtype, what=w.name)
+
+
+def _sample_rows(w, n_random=192, seed=0):
+    rng = np.random.default_rng(seed)
+    N, BH = w.N, w.B * w.H
+    special = [0, 1, 2, 127, 128, 129, 255, 256, 257, N // 2, N - 129, N - 128, N - 2, N - 1]
+    special = sorted({r for r in special if 0 <= r < N})
+    rows, bhs = [], []
+    for i, r in enumerate(special):
+        rows.append(r)
+        bhs.append(i % BH)
+    rows += list(rng.integers(0, N, n_random))
+    bhs += list(rng.integers(0, BH, n_random))
+    return np.array(bhs, np.int64), np.array(rows, np.int64)
+
+
+@pytest.mark.parametrize("name", sorted(n for n in fa_inputs.WORKLOADS if not n.startswith("tiny")))
+def test_full_size_workloads_sampled_rows(name):
+    w = fa_inputs.WORKLOADS[name]
+    q, k, v = fa_inputs.make_qkv(w, seed=0)
+    o, lse = _run(q, k, v, w.causal, w.scale)
+    bh, rows = _sample_rows(w)
+    o_ref, lse_ref = fa_ref.naive_rows(fa_inputs.bits(q), fa_inputs.bits(k), fa_inputs.bits(v), w.scale,
+                                       w.causal, bh, rows, enc=fa_inputs.enc(w))
+    o_s = o.reshape(w.B * w.H, w.N, w.D)[torch.from_numpy(bh).cuda(), torch.from_numpy(rows).cuda()]
+    l_s = lse.reshape(w.B * w.H, w.N)[torch.from_numpy(bh).cuda(), torch.from_numpy(rows).cuda()]
+    _check(o_s, l_s, o_ref, lse_ref, w.dtype, peaky=w.qk_std != 1.0, what=name)
+    # properties that hold for every row, checked on the whole output
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    if w.causal:
+        assert torch.equal(o[:, :, 0, :].cpu(), v[:, :, 0, :])   # row 0 sees only key 0
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_uniform_scores_give_mean_of_values(causal, dtype):
+    w = fa_inputs.Workload("uni", 1, 2, 700, 128, causal, dtype)
+    _, k, v = fa_inputs.make_qkv(w, seed=3)
+    q = torch.zeros_like(k)
+    o, lse = _run(q, k, v, causal, w.scale)
+    vd = v.double()
+    if causal:
+        want = vd.cumsum(2) / torch.arange(1, w.N + 1, dtype=torch.float64).view(1, 1, -1, 1)
+        want_lse = torch.log(torch.arange(1, w.N + 1, dtype=torch.float64)).expand(1, 2, -1)
+    else:
+        want = vd.mean(2, keepdim=True).expand_as(vd)
+        want_lse = torch.full((1, 2, w.N), float(np.log(w.N)), dtype=torch.float64)
+    _check(o, lse, want.numpy(), want_lse.numpy(), dtype, what="uniform")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_extreme_inputs_stay_finite(causal):
+    """fp16 max and mixed +-1e4 entries: the max subtraction keeps O finite."""
+    w = fa_inputs.Workload("ext", 1, 1, 300, 64, causal, "fp16")
+    g = torch.Generator().manual_seed(11)
+    choice = torch.tensor([-1e4, 1e4, 65504.0, 0.5], dtype=torch.float16)
+    q = choice[torch.randint(0, 4, (1, 1, 300, 64), generator=g)]
+    k = choice[torch.randint(0, 4, (1, 1, 300, 64), generator=g)]
+    v = torch.randn(1, 1, 300, 64, generator=g).half()
+    o, lse = _run(q, k, v, causal, 1.0 / 8)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    vmax, vmin = v.float().amax(2, keepdim=True).cuda(), v.float().amin(2, keepdim=True).cuda()
+    assert (o.float() <= vmax + 1e-3).all() and (o.float() >= vmin - 1e-3).all()
+
+
+def test_deterministic_and_stream_aware():
+    w = fa_inputs.WORKLOADS["causal_fp16_b1h32n1024d128"]
+    q, k, v = (t.cuda() for t in fa_inputs.make_qkv(w, seed=1))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1, l1 = fa.attention(q, k, v, causal=True, stream=s)
+        o2, l2 = fa.attention(q, k, v, causal=True, stream=s)
+    s.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert fa.fa_get_device_status(s.cuda_stream) == fa.FA_OK
+
+
+def test_bad_arguments_leave_outputs_untouched():
+    q = torch.randn(1, 1, 64, 96, device="cuda", dtype=torch.float16)
+    o = torch.full_like(q, 7.0)
+    lse = torch.full((1, 1, 64), 7.0, device="cuda")
+    st = fa.fa_fwd(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 64, 96, 0.1, 0,
+                   fa.FA_FP16, 0)
+    assert st == 2
+    torch.cuda.synchronize()
+    assert (o == 7).all() and (lse == 7).all()
+    assert fa.fa_get_device_status(0) == fa.FA_OK
