@@ -332,14 +332,8 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, int q0, int N
         float s[kTileN];
         tmem_ld128_wait(ts, s);
 
-        // Scale into log2 units first and take the max of those rounded values,
-        // so the row's largest element maps to exactly 2^0 however large the
-        // scores are (subtracting a separately rounded max inside one fma can
-        // leave an error of many units when |s| is huge).
         const int k0 = j * kTileN;
         const bool need_mask = (CAUSAL && j == nkv_t - 1) || (k0 + kTileN > N);
-#pragma unroll
-        for (int c = 0; c < kTileN; ++c) s[c] *= scale_log2;
         if (need_mask) {
 #pragma unroll
             for (int c = 0; c < kTileN; ++c) {
@@ -347,13 +341,18 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, int q0, int N
                 if (key >= N || (CAUSAL && key > qi)) s[c] = -INFINITY;
             }
         }
-        float mx[8];
+        // Row max of the raw scores (three-input max), then into log2 units.
+        float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-        for (int c = 8; c < kTileN; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-        const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int c = 4; c < kTileN; c += 8) {
+            mx[0] = fmax3(mx[0], s[c], s[c + 1]);
+            mx[1] = fmax3(mx[1], s[c + 2], s[c + 3]);
+            if (c + 4 < kTileN) {
+                mx[2] = fmax3(mx[2], s[c + 4], s[c + 5]);
+                mx[3] = fmax3(mx[3], s[c + 6], s[c + 7]);
+            }
+        }
+        const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * scale_log2;
         const float m_new = fmaxf(m_ref, m_tile);
         float alpha = 1.f;
         if (m_ref == -INFINITY) {
@@ -367,35 +366,60 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, int q0, int N
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.alpha_ready[t]);
 
+        // p = 2^(s*c - m_ref), one rounding of the fused product-difference.
+        // m_ref = round(max * c) is the same reference for every element of the
+        // row, so it need not equal the exact max: the row's largest element
+        // gets an exponent within half an ulp of m_ref of zero.  For
+        // |m_ref| >= 2^24 that half ulp is more than a unit and could overflow
+        // 16-bit P, so such rows round the product on its own and subtract
+        // after (then the largest element maps to exactly 2^0).
         const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float lt[4] = {0.f, 0.f, 0.f, 0.f};
-        float lx[4] = {0.f, 0.f, 0.f, 0.f};
+        const bool fused = fabsf(msub) < 16777216.f;
+        const uint64_t c2 = pack_f32x2(scale_log2, scale_log2);
+        const uint64_t nm2 = pack_f32x2(-msub, -msub);
+        float lr[4] = {0.f, 0.f, 0.f, 0.f};   // sums of the rounded 16-bit P
+        uint64_t lx2 = pack_f32x2(0.f, 0.f);   // sum of the fp32 p (bf16 only)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t pk[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float p0 = ex2_approx(s[64 * h + 2 * i] - msub);
-                const float p1 = ex2_approx(s[64 * h + 2 * i + 1] - msub);
+                float x0, x1;
+                if (fused) {
+                    const uint64_t s2 = pack_f32x2(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]);
+                    unpack_f32x2(fma_f32x2(s2, c2, nm2), x0, x1);
+                } else {
+                    // never contracted into an fma: the product is rounded on its own
+                    x0 = __fadd_rn(__fmul_rn(s[64 * h + 2 * i], scale_log2), -msub);
+                    x1 = __fadd_rn(__fmul_rn(s[64 * h + 2 * i + 1], scale_log2), -msub);
+                }
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                 uint32_t w;
-                float r0, r1;
                 if constexpr (BF16) {
                     w = pack_bf16x2(p0, p1);
-                    r0 = __uint_as_float(w << 16);
-                    r1 = __uint_as_float(w & 0xffff0000u);
+                    lr[i & 3] = add_lo_bf16(w, lr[i & 3]);
+                    lr[(i + 2) & 3] = add_hi_bf16(w, lr[(i + 2) & 3]);
+                    lx2 = add_f32x2(lx2, pack_f32x2(p0, p1));
                 } else {
                     w = pack_f16x2(p0, p1);
-                    r0 = __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
-                    r1 = __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+                    lr[i & 3] = add_lo_f16(w, lr[i & 3]);
+                    lr[(i + 2) & 3] = add_hi_f16(w, lr[(i + 2) & 3]);
                 }
                 pk[i] = w;
-                lt[i & 3] += r0 + r1;
-                lx[i & 3] += p0 + p1;
             }
             tmem_st32(ts + 32 * h, pk);
         }
-        l = l * alpha + ((lt[0] + lt[1]) + (lt[2] + lt[3]));
-        ls = ls * alpha + ((lx[0] + lx[1]) + (lx[2] + lx[3]));
+        const float l_tile = (lr[0] + lr[1]) + (lr[2] + lr[3]);
+        l = l * alpha + l_tile;
+        if constexpr (BF16) {
+            float x0, x1;
+            unpack_f32x2(lx2, x0, x1);
+            ls = ls * alpha + (x0 + x1);
+        } else {
+            // fp16 P is within 2^-11 of p, so the rounded sum also gives the
+            // log-sum-exp to better than 5e-4.
+            ls = l;
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
