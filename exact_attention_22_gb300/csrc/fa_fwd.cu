@@ -12,23 +12,24 @@
 // never visited.
 //
 // How it is computed is this file's own design for Blackwell:
-//   * one CTA = 256 query rows of one (b, h) = two 128-row Q tiles that share
-//     every K/V tile;
-//   * TMA loads Q once and streams K_j, V_j through a shared-memory ring
-//     (128-byte swizzle, mbarrier full/empty pairs);
+//   * a persistent grid, one CTA per SM; a work tile is 256 query rows of one
+//     (b, h) = two 128-row Q tiles ("streams" 0 and 1) that share every K/V
+//     tile; tiles are dealt heaviest first, in a snake order over the CTAs;
+//   * TMA loads each Q tile once and streams K_j, V_j through a shared-memory
+//     ring (128-byte swizzle, mbarrier full/empty pairs);
 //   * one thread issues tcgen05 UMMAs: S_t = Q_t K_j^T into tensor memory
 //     (TMEM), and O_t += P_t V_j with P_t read back from TMEM, where it
-//     overwrites the first half of S_t;
-//   * a softmax warpgroup per Q tile owns one row per thread: it loads the S
-//     row from TMEM, masks, takes the max, exponentiates in base 2 and writes
-//     P_t (16-bit) back to TMEM;
+//     overwrites the first half of S_t.  When a stream finishes its K/V tiles
+//     its next S is the first one of the CTA's next work tile, so the tensor
+//     core keeps alternating between the streams across tile boundaries;
+//   * a softmax warpgroup per stream owns one row per thread: it loads the S
+//     row from TMEM, masks, takes the max, exponentiates in base 2, writes
+//     P_t (16-bit) back to TMEM, and at the end of a work tile writes O / l
+//     and the LSE of its rows straight from registers;
 //   * a correction warpgroup rescales O_t in TMEM when a row's reference max
 //     moves by more than 2^8 (the reference may lag the true max: the
 //     invariant O = sum e^(s - m_ref) v, l = sum e^(s - m_ref) holds for any
-//     m_ref used consistently, so the result is unchanged), and finally
-//     writes O / l through a TMA store and LSE with plain stores;
-//   * the two Q tiles ping-pong: while one softmax warpgroup exponentiates,
-//     the tensor core works on the other tile.
+//     m_ref used consistently, so the result is unchanged).
 // Every mbarrier wait is bounded in time; a wait that gives up records a
 // status bit, makes the other roles stop, drains in-flight copies and MMAs,
 // frees TMEM and returns.
@@ -52,17 +53,18 @@ namespace fa103 {
 __device__ unsigned int g_fa_status;
 
 enum : unsigned {
-    ST_PRODUCER = 1u,
+    ST_KV_PRODUCER = 1u,
     ST_MMA = 2u,
     ST_SOFTMAX = 4u,
     ST_CORRECTION = 8u,
     ST_DRAIN = 16u,
+    ST_Q_PRODUCER = 32u,
 };
 
 constexpr int kTileM = 128;     // query rows of one Q tile (UMMA M)
 constexpr int kTileN = 128;     // keys of one K/V tile (UMMA N of S, K of P V)
-constexpr int kNumQ = 2;        // Q tiles per CTA
-constexpr int kRowsPerCta = kTileM * kNumQ;
+constexpr int kNumQ = 2;        // Q tiles (streams) per work tile
+constexpr int kRowsPerTile = kTileM * kNumQ;
 constexpr int kThreads = 128 * (2 + kNumQ);   // producer/MMA WG, softmax WGs, correction WG
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;   // 1 s per wait
 constexpr float kLazyRescale = 8.0f;          // log2 units: rescale only when the max grows > 2^8
@@ -70,7 +72,7 @@ constexpr uint32_t kTmemCols = 512;
 
 template <int D>
 struct Cfg {
-    static constexpr int kTileBytes = kTileM * D * 2;   // one 128-row tile of Q, K, V or O
+    static constexpr int kTileBytes = kTileM * D * 2;   // one 128-row tile of Q, K or V
     static constexpr int kBoxes = D / 64;               // 64-element (128-byte) swizzle boxes along D
     static constexpr int kBoxBytes = kTileM * 128;
     static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring slots
@@ -83,34 +85,67 @@ struct Cfg {
 };
 
 struct __align__(8) SharedState {
-    uint64_t q_full;
+    uint64_t q_full[kNumQ];        // Q producer -> MMA: Q_t of the current work tile landed
+    uint64_t q_empty[kNumQ];       // MMA -> Q producer: the last S_t of a work tile finished
     uint64_t kv_full[8];
     uint64_t kv_empty[8];
-    uint64_t s_full[kNumQ];        // MMA -> softmax: S_t of the current tile is in TMEM
-    uint64_t p_full[kNumQ];        // softmax -> MMA: P_t written to TMEM
+    uint64_t s_full[kNumQ];        // MMA -> softmax: S_t of the current step is in TMEM
+    uint64_t p_full[kNumQ];        // softmax + correction -> MMA: P_t in TMEM and O_t rescaled
     uint64_t alpha_ready[kNumQ];   // softmax -> correction: per-row rescale factors published
-    uint64_t o_ready[kNumQ];       // correction -> MMA: O_t rescaled, P_t V may accumulate
-    uint64_t pv_done[kNumQ];       // MMA -> correction: O_t += P_t V_j complete
-    uint64_t stats_ready[kNumQ];   // softmax -> epilogue: final m, l of every row
+    uint64_t pv_done[kNumQ];       // MMA -> softmax/correction: O_t += P_t V_j complete
     uint64_t drain;
     float alpha[kNumQ][kTileM];
-    float row_m[kNumQ][kTileM];
-    float row_l[kNumQ][kTileM];    // sum of the rounded P used by P V: normalises O
-    float row_ls[kNumQ][kTileM];   // sum of the fp32 p: the log-sum-exp
     uint32_t tmem_base;
     int abort_flag;
 };
 
 struct Params {
+    void* o;
     float* lse;
     int N;
     int BH;
     int n_qblocks;       // ceil(N / 256)
+    int n_tiles;         // n_qblocks * BH
     float scale_log2;    // scale * log2(e)
 };
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
+// One work tile: query rows q0 .. q0+255 of head bh.
+struct Tile {
+    int q0, bh, n_all;
+    int nkv[kNumQ];      // K/V tiles each stream visits (0: stream starts past N)
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Tile make_tile(const Params& p, int idx) {
+    Tile w;
+    // heaviest query block first: causal work grows with the block index
+    w.q0 = (p.n_qblocks - 1 - idx / p.BH) * kRowsPerTile;
+    w.bh = idx % p.BH;
+    w.n_all = 0;
+#pragma unroll
+    for (int t = 0; t < kNumQ; ++t) {
+        const int r0 = w.q0 + kTileM * t;
+        if (r0 >= p.N)
+            w.nkv[t] = 0;
+        else if (CAUSAL)
+            w.nkv[t] = min(r0 + kTileM - 1, p.N - 1) / kTileN + 1;
+        else
+            w.nkv[t] = (p.N + kTileN - 1) / kTileN;
+        w.n_all = max(w.n_all, w.nkv[t]);
+    }
+    return w;
+}
+
+// The k-th work tile of this CTA, or -1: rounds of gridDim.x tiles, dealt in a
+// snake order so a CTA that got a heavy tile in one round gets a light one in
+// the next.
+__device__ __forceinline__ int tile_index(int k, int n_tiles) {
+    const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+    const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
+    return idx < n_tiles ? static_cast<int>(idx) : -1;
+}
+
+__device__ __forceinline__ bool wait_bar_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
@@ -119,6 +154,11 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
     }
+}
+// Wait for the phase of `bar` with the given parity; false if it took longer
+// than the time-out or another role gave up meanwhile.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    return mbar_try_wait(bar, parity) || wait_bar_slow(bar, parity, abort_flag);
 }
 
 __device__ __forceinline__ void give_up(SharedState& sh, unsigned code) {
@@ -135,7 +175,7 @@ __device__ __forceinline__ void setmaxnreg_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N_));
 }
 
-// 128 consecutive TMEM columns of this thread's lane, one wait for all four loads.
+// 128 consecutive TMEM columns of this thread's lane, one wait for both loads.
 __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, float (&s)[128]) {
     uint32_t(&r)[128] = reinterpret_cast<uint32_t(&)[128]>(s);
     asm volatile(
@@ -175,132 +215,213 @@ __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, float (&s)[128])
 
 // ------------------------------------------------------------------ roles
 
-template <int D>
-__device__ void run_producer(SharedState& sh, uint8_t* tiles, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
-                             const CUtensorMap* tm_v, int q0, int bh, const int (&nkv)[kNumQ], int n_all) {
+// K/V producer: one thread; K_j then V_j of every work tile, in order.
+template <int D, bool CAUSAL>
+__device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                const Params& p) {
     using C = Cfg<D>;
     volatile int* abort_flag = &sh.abort_flag;
-    prefetch_tmap(tm_q);
     prefetch_tmap(tm_k);
     prefetch_tmap(tm_v);
-    const uint64_t pol_keep = l2_policy_evict_last();    // K, V: re-read by the head's other CTAs
-    const uint64_t pol_once = l2_policy_evict_first();   // Q: read once
-
-    int nq_active = 0;
-    for (int t = 0; t < kNumQ; ++t) nq_active += nkv[t] > 0;
-    mbar_arrive_expect_tx(&sh.q_full, nq_active * C::kTileBytes);
-    for (int t = 0; t < kNumQ; ++t) {
-        if (nkv[t] == 0) continue;
-        for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d_hint(tiles + C::kOffQ + t * C::kTileBytes + b * C::kBoxBytes, tm_q, &sh.q_full, 64 * b,
-                             q0 + kTileM * t, bh, pol_once);
-    }
-
-    int last_item[C::kStages];
-    for (int s = 0; s < C::kStages; ++s) last_item[s] = -1;
+    const uint64_t pol_keep = l2_policy_evict_last();   // K, V: re-read by the head's other work tiles
     int item = 0;
     bool ok = true;
-    for (int j = 0; j < n_all && ok; ++j) {
-        for (int kind = 0; kind < 2; ++kind, ++item) {   // K_j, then V_j
-            const int slot = item % C::kStages;
-            const uint32_t phase = (item / C::kStages) & 1;
-            if (!wait_bar(&sh.kv_empty[slot], phase ^ 1, abort_flag)) {
-                give_up(sh, ST_PRODUCER);
-                ok = false;
-                break;
+    for (int k = 0; ok; ++k) {
+        const int idx = tile_index(k, p.n_tiles);
+        if (idx < 0) break;
+        const Tile w = make_tile<CAUSAL>(p, idx);
+        for (int j = 0; j < w.n_all && ok; ++j) {
+#pragma unroll 1
+            for (int kind = 0; kind < 2; ++kind, ++item) {   // K_j, then V_j
+                const int slot = item % C::kStages;
+                if (!wait_bar(&sh.kv_empty[slot], ((item / C::kStages) & 1) ^ 1, abort_flag)) {
+                    give_up(sh, ST_KV_PRODUCER);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sh.kv_full[slot], C::kTileBytes);
+                const CUtensorMap* map = kind ? tm_v : tm_k;
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d_hint(tiles + C::kOffKV + slot * C::kTileBytes + b * C::kBoxBytes, map,
+                                     &sh.kv_full[slot], 64 * b, j * kTileN, w.bh, pol_keep);
             }
-            mbar_arrive_expect_tx(&sh.kv_full[slot], C::kTileBytes);
-            const CUtensorMap* map = kind ? tm_v : tm_k;
-            for (int b = 0; b < C::kBoxes; ++b)
-                tma_load_3d_hint(tiles + C::kOffKV + slot * C::kTileBytes + b * C::kBoxBytes, map,
-                                 &sh.kv_full[slot], 64 * b, j * kTileN, bh, pol_keep);
-            last_item[slot] = item;
         }
     }
     if (!ok) {
-        // Let every copy already issued land before the CTA's shared memory goes away.
+        // Let every copy already issued (items < item) land before the CTA's
+        // shared memory goes away: the last item of each slot is enough.
         volatile int never = 0;
-        wait_bar(&sh.q_full, 0, &never);
-        for (int s = 0; s < C::kStages; ++s)
-            if (last_item[s] >= 0) wait_bar(&sh.kv_full[s], (last_item[s] / C::kStages) & 1, &never);
+        for (int last = item - 1; last >= 0 && last >= item - C::kStages; --last)
+            wait_bar(&sh.kv_full[last % C::kStages], (last / C::kStages) & 1, &never);
     }
 }
 
-template <int D, bool BF16>
-__device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const int (&nkv)[kNumQ], int n_all) {
+// Q producer: one thread; Q_t of every work tile once its buffer is free.
+template <int D, bool CAUSAL>
+__device__ void run_q_producer(SharedState& sh, uint8_t* tiles, const CUtensorMap* tm_q, const Params& p) {
+    using C = Cfg<D>;
+    volatile int* abort_flag = &sh.abort_flag;
+    prefetch_tmap(tm_q);
+    const uint64_t pol_once = l2_policy_evict_first();   // Q: read once
+    int loads[kNumQ] = {0, 0};
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+        const int idx = tile_index(k, p.n_tiles);
+        if (idx < 0) break;
+        const Tile w = make_tile<CAUSAL>(p, idx);
+        for (int t = 0; t < kNumQ; ++t) {
+            if (w.nkv[t] == 0) continue;
+            if (!wait_bar(&sh.q_empty[t], (loads[t] & 1) ^ 1, abort_flag)) {
+                give_up(sh, ST_Q_PRODUCER);
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(&sh.q_full[t], C::kTileBytes);
+            for (int b = 0; b < C::kBoxes; ++b)
+                tma_load_3d_hint(tiles + C::kOffQ + t * C::kTileBytes + b * C::kBoxBytes, tm_q, &sh.q_full[t], 64 * b,
+                                 w.q0 + kTileM * t, w.bh, pol_once);
+            ++loads[t];
+        }
+    }
+    if (!ok) {
+        volatile int never = 0;
+        for (int t = 0; t < kNumQ; ++t)
+            if (loads[t] > 0) wait_bar(&sh.q_full[t], (loads[t] - 1) & 1, &never);
+    }
+}
+
+// UMMA issuer: one thread.
+//
+// Ring items are K_0, V_0, K_1, V_1, ... of each work tile in turn; they are
+// acquired (full barrier waited) in that order.  An item is released (empty
+// barrier committed after the MMA that reads it) by the last stream that
+// reads it: stream 1, or stream 0 where stream 1 does not visit that K/V tile.
+template <int D, bool BF16, bool CAUSAL>
+__device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Params& p) {
     using C = Cfg<D>;
     volatile int* abort_flag = &sh.abort_flag;
     constexpr uint32_t kIdS = idesc_f16(BF16, kTileM, kTileN, false);
     constexpr uint32_t kIdO = idesc_f16(BF16, kTileM, D, true);
-    const uint32_t sq = smem_u32(tiles + C::kOffQ);
-    const uint32_t skv = smem_u32(tiles + C::kOffKV);
+    // Descriptors are built once per operand; a K-step only moves the start
+    // address field (address / 16, the low bits of the descriptor), which never
+    // carries out for shared-memory addresses.
+    const uint64_t dq0 = sdesc_sw128(smem_u32(tiles + C::kOffQ), 16, 1024);
+    const uint64_t dkv0 = sdesc_sw128(smem_u32(tiles + C::kOffKV), 16, 1024);
+    const uint64_t dv0 = sdesc_sw128(smem_u32(tiles + C::kOffKV), C::kBoxBytes, 1024);
 
-    auto issue_s = [&](int t, int slot) {
-        const uint32_t qa = sq + t * C::kTileBytes, kb = skv + slot * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-            umma_ss(tmem + C::tm_s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), kIdS,
-                    kk > 0);
-        }
-    };
-    auto issue_pv = [&](int t, int slot, bool first) {
-        const uint32_t vb = skv + slot * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk)
-            umma_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + kk * 8, sdesc_sw128(vb + kk * 2048, C::kBoxBytes, 1024),
-                    kIdO, !(first && kk == 0));
-    };
-    auto ring_wait = [&](int item) -> bool {
-        return wait_bar(&sh.kv_full[item % C::kStages], (item / C::kStages) & 1, abort_flag);
-    };
+    int acquired = 0;        // ring items acquired so far
+    uint32_t pv_par = 0;     // bit t: parity of stream t's next p_full phase
+    uint32_t q_par = 0;      // bit t: parity of stream t's next q_full phase
+    bool ok = true;
 
-    bool ok = wait_bar(&sh.q_full, 0, abort_flag);
-    int item = 0;
-    if (ok) ok = ring_wait(item);   // K_0
-    if (ok) {
+    auto acquire = [&](int it) -> bool {
+        if (acquired > it) return true;
+        do {
+            if (!wait_bar(&sh.kv_full[acquired % C::kStages], (acquired / C::kStages) & 1, abort_flag)) return false;
+        } while (++acquired <= it);
         tc_fence_after();
-        const int slot = item % C::kStages;
+        return true;
+    };
+    auto issue_s = [&](int t, int item, bool release) {
+        const uint64_t da = dq0 + ((t * C::kTileBytes) >> 4);
+        const uint64_t db = dkv0 + (((item % C::kStages) * C::kTileBytes) >> 4);
+        const uint32_t d = tmem + C::tm_s(t);
+        // K-step kk reads 16 columns of D: 32 bytes into a 128-byte row, in box kk / 4
+        umma_ss_off<0, 0>(d, da, db, kIdS, 0);
+        umma_ss_off<2, 2>(d, da, db, kIdS, 1);
+        umma_ss_off<4, 4>(d, da, db, kIdS, 1);
+        umma_ss_off<6, 6>(d, da, db, kIdS, 1);
+        if constexpr (D == 128) {
+            constexpr uint32_t B = C::kBoxBytes >> 4;
+            umma_ss_off<B + 0, B + 0>(d, da, db, kIdS, 1);
+            umma_ss_off<B + 2, B + 2>(d, da, db, kIdS, 1);
+            umma_ss_off<B + 4, B + 4>(d, da, db, kIdS, 1);
+            umma_ss_off<B + 6, B + 6>(d, da, db, kIdS, 1);
+        }
+        umma_commit(&sh.s_full[t]);
+        if (release) umma_commit(&sh.kv_empty[item % C::kStages]);
+    };
+    auto issue_pv = [&](int t, int item, bool first, bool release) {
+        const uint64_t dv = dv0 + (((item % C::kStages) * C::kTileBytes) >> 4);
+        const uint32_t d = tmem + C::tm_o(t), a = tmem + C::tm_s(t);
+        // K-step kk reads 16 keys = 2048 bytes of V and 8 TMEM columns of P
+        umma_ts_off<0 * 128>(d, a + 0, dv, kIdO, first ? 0u : 1u);
+        umma_ts_off<1 * 128>(d, a + 8, dv, kIdO, 1);
+        umma_ts_off<2 * 128>(d, a + 16, dv, kIdO, 1);
+        umma_ts_off<3 * 128>(d, a + 24, dv, kIdO, 1);
+        umma_ts_off<4 * 128>(d, a + 32, dv, kIdO, 1);
+        umma_ts_off<5 * 128>(d, a + 40, dv, kIdO, 1);
+        umma_ts_off<6 * 128>(d, a + 48, dv, kIdO, 1);
+        umma_ts_off<7 * 128>(d, a + 56, dv, kIdO, 1);
+        umma_commit(&sh.pv_done[t]);
+        if (release) umma_commit(&sh.kv_empty[item % C::kStages]);
+    };
+    // First S of stream t in work tile w (ring items from `base`).
+    auto start_stream = [&](int t, const Tile& w, int base) -> bool {
+        if (!wait_bar(&sh.q_full[t], (q_par >> t) & 1, abort_flag)) return false;
+        q_par ^= 1u << t;
+        if (!acquire(base)) return false;
+        issue_s(t, base, t == kNumQ - 1 || w.nkv[kNumQ - 1] == 0);
+        if (w.nkv[t] == 1) umma_commit(&sh.q_empty[t]);   // that was its last S of this work tile
+        return true;
+    };
+
+    int k = 0;
+    int idx = tile_index(0, p.n_tiles);
+    if (idx < 0) return;
+    Tile cur = make_tile<CAUSAL>(p, idx);
+    int cur_base = 0;
+    uint32_t started = 0;    // bit t: first S of `cur` already issued by the previous tile
+    while (ok) {
+        const int nidx = tile_index(k + 1, p.n_tiles);
+        const bool has_next = nidx >= 0;
+        const Tile nxt = has_next ? make_tile<CAUSAL>(p, nidx) : cur;
+        const int nxt_base = cur_base + 2 * cur.n_all;
+#pragma unroll
         for (int t = 0; t < kNumQ; ++t)
-            if (nkv[t] > 0) {
-                issue_s(t, slot);
-                umma_commit(&sh.s_full[t]);
-            }
-        umma_commit(&sh.kv_empty[slot]);
-        ++item;
-    }
-    for (int j = 0; j < n_all && ok; ++j) {
-        const int item_v = item++;
-        if (!ring_wait(item_v)) { ok = false; break; }
-        const int slot_v = item_v % C::kStages;
-        const bool has_next = j + 1 < n_all;
-        const int item_k = has_next ? item++ : -1;
-        bool k_ready = false;
-        for (int t = 0; t < kNumQ && ok; ++t) {
-            if (j >= nkv[t]) continue;
-            if (!wait_bar(&sh.p_full[t], j & 1, abort_flag) || !wait_bar(&sh.o_ready[t], j & 1, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            issue_pv(t, slot_v, j == 0);
-            umma_commit(&sh.pv_done[t]);
-            if (j + 1 < nkv[t]) {
-                if (!k_ready) {
-                    if (!ring_wait(item_k)) { ok = false; break; }
+            if (ok && cur.nkv[t] > 0 && !((started >> t) & 1)) ok = start_stream(t, cur, cur_base);
+        uint32_t nstarted = 0;
+        for (int j = 0; j < cur.n_all && ok; ++j) {
+#pragma unroll
+            for (int t = 0; t < kNumQ; ++t) {
+                if (!ok || j >= cur.nkv[t]) continue;
+                const int item_v = cur_base + 2 * j + 1;
+                const bool more = j + 1 < cur.nkv[t];
+                // V_j, K_{j+1} (long since landed) and P_t: the three barriers
+                // are tested together so their latencies overlap; only a test
+                // that fails falls back to a bounded wait.
+                const int need = more ? item_v + 1 : item_v;
+                const int item_k = more ? item_v + 1 : item_v;
+                const uint32_t got = mbar_test3(&sh.kv_full[item_v % C::kStages], (item_v / C::kStages) & 1,
+                                                &sh.kv_full[item_k % C::kStages], (item_k / C::kStages) & 1,
+                                                &sh.p_full[t], (pv_par >> t) & 1);
+                const bool r_p = (got & 4u) != 0;
+                if ((got & 3u) == 3u && acquired >= item_v && acquired <= need) {
+                    acquired = need + 1;   // both tested complete above
                     tc_fence_after();
-                    k_ready = true;
                 }
-                issue_s(t, item_k % C::kStages);
-                umma_commit(&sh.s_full[t]);
+                if (!acquire(need) || (!r_p && !wait_bar(&sh.p_full[t], (pv_par >> t) & 1, abort_flag))) {
+                    ok = false;
+                    continue;
+                }
+                tc_fence_after();
+                pv_par ^= 1u << t;
+                issue_pv(t, item_v, j == 0, t == kNumQ - 1 || j >= cur.nkv[kNumQ - 1]);
+                if (more) {
+                    const int item_k = item_v + 1;
+                    issue_s(t, item_k, t == kNumQ - 1 || j + 1 >= cur.nkv[kNumQ - 1]);
+                    if (j + 2 == cur.nkv[t]) umma_commit(&sh.q_empty[t]);
+                } else if (has_next && nxt.nkv[t] > 0) {
+                    ok = start_stream(t, nxt, nxt_base);
+                    nstarted |= 1u << t;
+                }
             }
         }
-        if (!ok) break;
-        umma_commit(&sh.kv_empty[slot_v]);
-        if (has_next) {
-            if (!k_ready && !ring_wait(item_k)) { ok = false; break; }
-            umma_commit(&sh.kv_empty[item_k % C::kStages]);
-        }
+        if (!ok || !has_next) break;
+        ++k;
+        cur = nxt;
+        cur_base = nxt_base;
+        started = nstarted;
     }
     if (!ok) give_up(sh, ST_MMA);
     // Nothing of ours may still be in flight when the CTA retires.
@@ -310,272 +431,238 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const in
 }
 
 template <int D, bool BF16, bool CAUSAL>
-__device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, int q0, int N, float scale_log2, int nkv_t) {
+__device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params& p) {
     volatile int* abort_flag = &sh.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = threadIdx.x - 128 * (1 + t);               // row of this thread in Q tile t
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t ts = tmem + lane_addr + Cfg<D>::tm_s(t);
-    const int qi = q0 + kTileM * t + r;                       // global query index
+    const uint32_t to = tmem + lane_addr + Cfg<D>::tm_o(t);
+    const float scale_log2 = p.scale_log2;
+    const int N = p.N;
+    int step = 0;   // S/P steps of this stream so far (phase of s_full / p_full / alpha_ready / pv_done)
+    bool ok = true;
 
-    float m_ref = -INFINITY;   // reference max, log2 units of the scaled score
-    float l = 0.f;             // running sum of the 16-bit-rounded P actually used by P V
-    float ls = 0.f;            // running sum of the unrounded p, for the log-sum-exp
-    for (int j = 0; j < nkv_t; ++j) {
-        bool ok = wait_bar(&sh.s_full[t], j & 1, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) {
-            give_up(sh, ST_SOFTMAX);
-            break;
-        }
-        tc_fence_after();
-        float s[kTileN];
-        tmem_ld128_wait(ts, s);
+    for (int k = 0; ok; ++k) {
+        const int idx = tile_index(k, p.n_tiles);
+        if (idx < 0) break;
+        const Tile w = make_tile<CAUSAL>(p, idx);
+        const int nkv_t = w.nkv[t];
+        if (nkv_t == 0) continue;
+        const int qi = w.q0 + kTileM * t + r;                 // global query index of this row
 
-        const int k0 = j * kTileN;
-        const bool need_mask = (CAUSAL && j == nkv_t - 1) || (k0 + kTileN > N);
-        if (need_mask) {
+        float m_ref = -INFINITY;   // reference max, log2 units of the scaled score
+        float l = 0.f;             // running sum of the 16-bit-rounded P actually used by P V
+        float ls = 0.f;            // running sum of the unrounded p, for the log-sum-exp (bf16)
+        for (int j = 0; j < nkv_t; ++j, ++step) {
+            ok = __all_sync(0xffffffffu, wait_bar(&sh.s_full[t], step & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            float s[kTileN];
+            tmem_ld128_wait(ts, s);
+
+            const int k0 = j * kTileN;
+            const bool need_mask = (CAUSAL && j == nkv_t - 1) || (k0 + kTileN > N);
+            if (need_mask) {
 #pragma unroll
-            for (int c = 0; c < kTileN; ++c) {
-                const int key = k0 + c;
-                if (key >= N || (CAUSAL && key > qi)) s[c] = -INFINITY;
+                for (int c = 0; c < kTileN; ++c) {
+                    const int key = k0 + c;
+                    if (key >= N || (CAUSAL && key > qi)) s[c] = -INFINITY;
+                }
             }
-        }
-        // Row max of the raw scores (three-input max), then into log2 units.
-        float mx[4] = {s[0], s[1], s[2], s[3]};
+            // Row max of the raw scores (three-input max), then into log2 units.
+            float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int c = 4; c < kTileN; c += 8) {
-            mx[0] = fmax3(mx[0], s[c], s[c + 1]);
-            mx[1] = fmax3(mx[1], s[c + 2], s[c + 3]);
-            if (c + 4 < kTileN) {
-                mx[2] = fmax3(mx[2], s[c + 4], s[c + 5]);
-                mx[3] = fmax3(mx[3], s[c + 6], s[c + 7]);
+            for (int c = 4; c < kTileN; c += 8) {
+                mx[0] = fmax3(mx[0], s[c], s[c + 1]);
+                mx[1] = fmax3(mx[1], s[c + 2], s[c + 3]);
+                if (c + 4 < kTileN) {
+                    mx[2] = fmax3(mx[2], s[c + 4], s[c + 5]);
+                    mx[3] = fmax3(mx[3], s[c + 6], s[c + 7]);
+                }
             }
-        }
-        const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * scale_log2;
-        const float m_new = fmaxf(m_ref, m_tile);
-        float alpha = 1.f;
-        if (m_ref == -INFINITY) {
-            alpha = 0.f;            // nothing accumulated yet
-            m_ref = m_new;
-        } else if (m_new > m_ref + kLazyRescale) {
-            alpha = ex2_approx(m_ref - m_new);
-            m_ref = m_new;
-        }
-        sh.alpha[t][r] = alpha;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.alpha_ready[t]);
+            const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * scale_log2;
+            const float m_new = fmaxf(m_ref, m_tile);
+            float alpha = 1.f;
+            if (m_ref == -INFINITY) {
+                alpha = 0.f;            // nothing accumulated yet
+                m_ref = m_new;
+            } else if (m_new > m_ref + kLazyRescale) {
+                alpha = ex2_approx(m_ref - m_new);
+                m_ref = m_new;
+            }
+            sh.alpha[t][r] = alpha;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.alpha_ready[t]);
 
-        // p = 2^(s*c - m_ref), one rounding of the fused product-difference.
-        // m_ref = round(max * c) is the same reference for every element of the
-        // row, so it need not equal the exact max: the row's largest element
-        // gets an exponent within half an ulp of m_ref of zero.  For
-        // |m_ref| >= 2^24 that half ulp is more than a unit and could overflow
-        // 16-bit P, so such rows round the product on its own and subtract
-        // after (then the largest element maps to exactly 2^0).
-        const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const bool fused = fabsf(msub) < 16777216.f;
-        const uint64_t c2 = pack_f32x2(scale_log2, scale_log2);
-        const uint64_t nm2 = pack_f32x2(-msub, -msub);
-        float lr[4] = {0.f, 0.f, 0.f, 0.f};   // sums of the rounded 16-bit P
-        uint64_t lx2 = pack_f32x2(0.f, 0.f);   // sum of the fp32 p (bf16 only)
+            // p = 2^(s*c - m_ref), one rounding of the fused product-difference.
+            // m_ref = round(max * c) is the same reference for every element of
+            // the row, so it need not equal the exact max: the row's largest
+            // element gets an exponent within half an ulp of m_ref of zero.  For
+            // |m_ref| >= 2^24 that half ulp is more than a unit and could
+            // overflow 16-bit P, so such rows round the product on its own and
+            // subtract after (then the largest element maps to exactly 2^0).
+            const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
+            const bool fused = fabsf(msub) < 16777216.f;
+            const uint64_t c2 = pack_f32x2(scale_log2, scale_log2);
+            const uint64_t nm2 = pack_f32x2(-msub, -msub);
+            uint64_t lx2 = pack_f32x2(0.f, 0.f);   // sum of the fp32 p (bf16 only)
+            uint32_t pk[kTileN / 2];                 // P as packed 16-bit pairs
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kTileN / 2; ++i) {
                 float x0, x1;
                 if (fused) {
-                    const uint64_t s2 = pack_f32x2(s[64 * h + 2 * i], s[64 * h + 2 * i + 1]);
+                    const uint64_t s2 = pack_f32x2(s[2 * i], s[2 * i + 1]);
                     unpack_f32x2(fma_f32x2(s2, c2, nm2), x0, x1);
                 } else {
                     // never contracted into an fma: the product is rounded on its own
-                    x0 = __fadd_rn(__fmul_rn(s[64 * h + 2 * i], scale_log2), -msub);
-                    x1 = __fadd_rn(__fmul_rn(s[64 * h + 2 * i + 1], scale_log2), -msub);
+                    x0 = __fadd_rn(__fmul_rn(s[2 * i], scale_log2), -msub);
+                    x1 = __fadd_rn(__fmul_rn(s[2 * i + 1], scale_log2), -msub);
                 }
                 const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                uint32_t w;
                 if constexpr (BF16) {
-                    w = pack_bf16x2(p0, p1);
-                    lr[i & 3] = add_lo_bf16(w, lr[i & 3]);
-                    lr[(i + 2) & 3] = add_hi_bf16(w, lr[(i + 2) & 3]);
+                    pk[i] = pack_bf16x2(p0, p1);
                     lx2 = add_f32x2(lx2, pack_f32x2(p0, p1));
                 } else {
-                    w = pack_f16x2(p0, p1);
-                    lr[i & 3] = add_lo_f16(w, lr[i & 3]);
-                    lr[(i + 2) & 3] = add_hi_f16(w, lr[(i + 2) & 3]);
+                    pk[i] = pack_f16x2(p0, p1);
                 }
-                pk[i] = w;
             }
-            tmem_st32(ts + 32 * h, pk);
+            tmem_st32(ts, reinterpret_cast<const uint32_t(&)[32]>(pk[0]));
+            tmem_st32(ts + 32, reinterpret_cast<const uint32_t(&)[32]>(pk[32]));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.p_full[t]);
+
+            // The row sums are not needed by the tensor core: they run while it
+            // does this stream's P V and next S.
+            float lr[4] = {0.f, 0.f, 0.f, 0.f};     // sums of the rounded 16-bit P
+#pragma unroll
+            for (int i = 0; i < kTileN / 2; ++i) {
+                if constexpr (BF16) {
+                    lr[i & 3] = add_lo_bf16(pk[i], lr[i & 3]);
+                    lr[(i + 2) & 3] = add_hi_bf16(pk[i], lr[(i + 2) & 3]);
+                } else {
+                    lr[i & 3] = add_lo_f16(pk[i], lr[i & 3]);
+                    lr[(i + 2) & 3] = add_hi_f16(pk[i], lr[(i + 2) & 3]);
+                }
+            }
+            l = l * alpha + ((lr[0] + lr[1]) + (lr[2] + lr[3]));
+            if constexpr (BF16) {
+                float x0, x1;
+                unpack_f32x2(lx2, x0, x1);
+                ls = ls * alpha + (x0 + x1);
+            } else {
+                // fp16 P is within 2^-11 of p, so the rounded sum also gives the
+                // log-sum-exp to better than 5e-4.
+                ls = l;
+            }
         }
-        const float l_tile = (lr[0] + lr[1]) + (lr[2] + lr[3]);
-        l = l * alpha + l_tile;
-        if constexpr (BF16) {
-            float x0, x1;
-            unpack_f32x2(lx2, x0, x1);
-            ls = ls * alpha + (x0 + x1);
-        } else {
-            // fp16 P is within 2^-11 of p, so the rounded sum also gives the
-            // log-sum-exp to better than 5e-4.
-            ls = l;
+        if (!ok) break;
+
+        // Epilogue of this work tile: wait for the last P V, then O / l -> 16-bit
+        // -> global (rows past N are not written) and the LSE.
+        ok = __all_sync(0xffffffffu, wait_bar(&sh.pv_done[t], (step - 1) & 1, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const bool row_ok = qi < N;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                               (static_cast<size_t>(w.bh) * N + (row_ok ? qi : 0)) * D);
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+            uint32_t v[32];
+            tmem_ld32_wait(to + c, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float x0 = __uint_as_float(v[2 * i]) * inv, x1 = __uint_as_float(v[2 * i + 1]) * inv;
+                pk[i] = BF16 ? pack_bf16x2(x0, x1) : pack_f16x2(x0, x1);
+            }
+            if (row_ok) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    orow[c / 8 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
         }
-        tmem_st_wait();
+        if (row_ok)
+            p.lse[static_cast<size_t>(w.bh) * N + qi] =
+                ls > 0.f ? (m_ref + log2f(ls)) * 0.69314718055994531f : -INFINITY;
+        // The next work tile's first P V overwrites O_t; it waits for this
+        // stream's next p_full, which comes after these loads.
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.p_full[t]);
     }
-    sh.row_m[t][r] = m_ref;
-    sh.row_l[t][r] = l;
-    sh.row_ls[t][r] = ls;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.stats_ready[t]);
+    if (!ok) give_up(sh, ST_SOFTMAX);
 }
 
-// Named barrier over the correction warpgroup whose result is the OR of `pred`.
-__device__ __forceinline__ bool wg_any(bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.cta.red.or.pred q, 1, 128, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred))
-        : "memory");
-    return r != 0;
-}
-
-template <int D, bool BF16>
-__device__ void run_correction(SharedState& sh, uint8_t* tiles, uint32_t tmem, const CUtensorMap* tm_o,
-                               const Params& p, int q0, int bh, const int (&nkv)[kNumQ], int n_all) {
+template <int D, bool CAUSAL>
+__device__ void run_correction(SharedState& sh, uint32_t tmem, const Params& p) {
     using C = Cfg<D>;
     volatile int* abort_flag = &sh.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = threadIdx.x - 128 * (1 + kNumQ);
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-
+    int steps[kNumQ] = {0, 0};
     bool ok = true;
-    for (int j = 0; j < n_all && ok; ++j) {
-        for (int t = 0; t < kNumQ; ++t) {
-            if (j >= nkv[t]) continue;
-            ok = __all_sync(0xffffffffu, wait_bar(&sh.alpha_ready[t], j & 1, abort_flag));
-            if (!ok) break;
-            if (j > 0) {
-                const float a = sh.alpha[t][r];
-                if (__any_sync(0xffffffffu, a != 1.f)) {
-                    // O_t holds P V of tiles 0..j-1; its last update finished before S_t(j) did.
-                    ok = __all_sync(0xffffffffu, wait_bar(&sh.pv_done[t], (j - 1) & 1, abort_flag));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t to = tmem + lane_addr + C::tm_o(t);
+    for (int k = 0; ok; ++k) {
+        const int idx = tile_index(k, p.n_tiles);
+        if (idx < 0) break;
+        const Tile w = make_tile<CAUSAL>(p, idx);
+        for (int j = 0; j < w.n_all && ok; ++j) {
+            for (int t = 0; t < kNumQ; ++t) {
+                if (j >= w.nkv[t]) continue;
+                ok = __all_sync(0xffffffffu, wait_bar(&sh.alpha_ready[t], steps[t] & 1, abort_flag));
+                if (!ok) break;
+                if (j > 0) {
+                    const float a = sh.alpha[t][r];
+                    if (__any_sync(0xffffffffu, a != 1.f)) {
+                        // O_t holds P V of steps < j; the last of them finished before S_t(j) did.
+                        ok = __all_sync(0xffffffffu, wait_bar(&sh.pv_done[t], (steps[t] - 1) & 1, abort_flag));
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t to = tmem + lane_addr + C::tm_o(t);
 #pragma unroll
-                    for (int c = 0; c < D; c += 32) {
-                        uint32_t v[32];
-                        tmem_ld32_wait(to + c, v);
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t v[32];
+                            tmem_ld32_wait(to + c, v);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
-                        tmem_st32(to + c, v);
+                            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+                            tmem_st32(to + c, v);
+                        }
+                        tmem_st_wait();
                     }
-                    tmem_st_wait();
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.p_full[t]);
+                ++steps[t];
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.o_ready[t]);
         }
     }
     if (!ok) give_up(sh, ST_CORRECTION);
-
-    // Epilogue: O / l -> 16-bit -> swizzled staging (the Q tile's buffer) -> TMA store; LSE.
-    bool stored = false;
-    for (int t = 0; t < kNumQ; ++t) {
-        if (nkv[t] == 0) continue;
-        bool good = ok && __all_sync(0xffffffffu, wait_bar(&sh.stats_ready[t], 0, abort_flag));
-        good = good && __all_sync(0xffffffffu, wait_bar(&sh.pv_done[t], (nkv[t] - 1) & 1, abort_flag));
-        uint8_t* stage = tiles + C::kOffQ + t * C::kTileBytes;
-        const int r0 = q0 + kTileM * t;
-        if (good) {
-            tc_fence_after();
-            const float m = sh.row_m[t][r], l = sh.row_l[t][r], ls = sh.row_ls[t][r];
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const uint32_t to = tmem + lane_addr + C::tm_o(t);
-#pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                uint32_t v[32];
-                tmem_ld32_wait(to + c, v);
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float x0 = __uint_as_float(v[2 * i]) * inv, x1 = __uint_as_float(v[2 * i + 1]) * inv;
-                    pk[i] = BF16 ? pack_bf16x2(x0, x1) : pack_f16x2(x0, x1);
-                }
-                const int box = c / 64;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chunk = (c % 64) / 8 + q;                     // 16-byte chunk within the 128-B row
-                    uint8_t* dst = stage + box * C::kBoxBytes + r * 128 + ((chunk ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                }
-            }
-            const int row = r0 + r;
-            if (row < p.N)
-                p.lse[static_cast<size_t>(bh) * p.N + row] =
-                    ls > 0.f ? (m + log2f(ls)) * 0.69314718055994531f : -INFINITY;
-            fence_proxy_async_smem();
-        }
-        const bool any_bad = wg_any(!good);
-        if (!any_bad && r == 0) {
-            for (int b = 0; b < C::kBoxes; ++b) tma_store_3d(tm_o, stage + b * C::kBoxBytes, 64 * b, r0, bh);
-            bulk_commit();
-            stored = true;
-        }
-        if (any_bad) ok = false;
-    }
-    if (stored) bulk_wait_all();
 }
 
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                  const Params p) {
+                  const __grid_constant__ CUtensorMap tm_v, const Params p) {
     extern __shared__ uint8_t dyn_smem[];
     __shared__ SharedState sh;
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, wg = warp >> 2;
 
-    // Heaviest query blocks first (causal work grows with the block index).
-    const int qb = p.n_qblocks - 1 - static_cast<int>(blockIdx.x / p.BH);
-    const int bh = static_cast<int>(blockIdx.x % p.BH);
-    const int q0 = qb * kRowsPerCta;
-    int nkv[kNumQ];
-    int n_all = 0;
-#pragma unroll
-    for (int t = 0; t < kNumQ; ++t) {
-        const int r0 = q0 + kTileM * t;
-        if (r0 >= p.N)
-            nkv[t] = 0;
-        else if (CAUSAL)
-            nkv[t] = min(r0 + kTileM - 1, p.N - 1) / kTileN + 1;
-        else
-            nkv[t] = (p.N + kTileN - 1) / kTileN;
-        n_all = max(n_all, nkv[t]);
-    }
-
     if (threadIdx.x == 0) {
-        mbar_init(&sh.q_full, 1);
+        for (int t = 0; t < kNumQ; ++t) {
+            mbar_init(&sh.q_full[t], 1);
+            mbar_init(&sh.q_empty[t], 1);
+            mbar_init(&sh.s_full[t], 1);
+            mbar_init(&sh.p_full[t], 8);   // 4 softmax warps + 4 correction warps
+            mbar_init(&sh.alpha_ready[t], 4);
+            mbar_init(&sh.pv_done[t], 1);
+        }
         for (int s = 0; s < Cfg<D>::kStages; ++s) {
             mbar_init(&sh.kv_full[s], 1);
             mbar_init(&sh.kv_empty[s], 1);
-        }
-        for (int t = 0; t < kNumQ; ++t) {
-            mbar_init(&sh.s_full[t], 1);
-            mbar_init(&sh.p_full[t], 4);
-            mbar_init(&sh.alpha_ready[t], 4);
-            mbar_init(&sh.o_ready[t], 4);
-            mbar_init(&sh.pv_done[t], 1);
-            mbar_init(&sh.stats_ready[t], 4);
         }
         mbar_init(&sh.drain, 1);
         sh.abort_flag = 0;
@@ -591,19 +678,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sh.tmem_base;
 
     if (wg == 0) {
-        setmaxnreg_dec<48>();
+        setmaxnreg_dec<96>();
         if (warp == 0 && lane == 0)
-            run_producer<D>(sh, tiles, &tm_q, &tm_k, &tm_v, q0, bh, nkv, n_all);
+            run_kv_producer<D, CAUSAL>(sh, tiles, &tm_k, &tm_v, p);
         else if (warp == 1 && lane == 0)
-            run_mma<D, BF16>(sh, tiles, tmem, nkv, n_all);
+            run_mma<D, BF16, CAUSAL>(sh, tiles, tmem, p);
+        else if (warp == 2 && lane == 0)
+            run_q_producer<D, CAUSAL>(sh, tiles, &tm_q, p);
         __syncwarp();
     } else if (wg <= kNumQ) {
-        setmaxnreg_inc<192>();
-        const int t = wg - 1;
-        if (nkv[t] > 0) run_softmax<D, BF16, CAUSAL>(sh, tmem, t, q0, p.N, p.scale_log2, nkv[t]);
+        setmaxnreg_inc<176>();
+        run_softmax<D, BF16, CAUSAL>(sh, tmem, wg - 1, p);
     } else {
-        setmaxnreg_dec<80>();
-        run_correction<D, BF16>(sh, tiles, tmem, &tm_o, p, q0, bh, nkv, n_all);
+        setmaxnreg_dec<64>();
+        run_correction<D, CAUSAL>(sh, tmem, p);
     }
 
     tc_fence_before();
@@ -646,9 +734,22 @@ static bool make_tile_map(CUtensorMap* map, const void* base, int dtype, int D, 
     return r == CUDA_SUCCESS;
 }
 
+// Streaming multiprocessors of a device (cached per device).
+static int sm_count(int dev) {
+    static std::atomic<int> cache[64];
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load();
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return -1;
+    if (dev >= 0 && dev < 64) cache[dev].store(n);
+    return n;
+}
+
 template <int D, bool BF16, bool CAUSAL>
-static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
-                          const Params& p, cudaStream_t stream) {
+static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
+                          cudaStream_t stream) {
     auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
     static std::atomic<uint64_t> configured{0};   // one bit per device
     int dev = 0;
@@ -660,8 +761,10 @@ static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    const unsigned grid = static_cast<unsigned>(p.n_qblocks) * static_cast<unsigned>(p.BH);
-    kern<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(q, k, v, o, p);
+    const int sms = sm_count(dev);
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const unsigned grid = static_cast<unsigned>(p.n_tiles < sms ? p.n_tiles : sms);
+    kern<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 
@@ -687,7 +790,7 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
     const uint64_t BH = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
     const uint64_t elems = BH * static_cast<uint64_t>(N) * static_cast<uint64_t>(D);
     if (BH > 0x7fffffffull || elems >= (uint64_t(1) << 40)) return FA_ERR_INVALID_ARG;
-    const uint64_t n_qblocks = (static_cast<uint64_t>(N) + kRowsPerCta - 1) / kRowsPerCta;
+    const uint64_t n_qblocks = (static_cast<uint64_t>(N) + kRowsPerTile - 1) / kRowsPerTile;
     if (n_qblocks * BH > 0x7fffffffull) return FA_ERR_INVALID_ARG;
     const size_t tbytes = static_cast<size_t>(elems) * 2, lbytes = static_cast<size_t>(BH) * N * sizeof(float);
     const void* ins[3] = {q, k, v};
@@ -695,22 +798,24 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
         if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes)) return FA_ERR_INVALID_ARG;
     if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
 
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     const int bh = static_cast<int>(BH);
     if (!make_tile_map(&mq, q, dtype, D, N, bh) || !make_tile_map(&mk, k, dtype, D, N, bh) ||
-        !make_tile_map(&mv, v, dtype, D, N, bh) || !make_tile_map(&mo, o, dtype, D, N, bh))
+        !make_tile_map(&mv, v, dtype, D, N, bh))
         return FA_ERR_CUDA;
 
     Params p;
+    p.o = o;
     p.lse = lse;
     p.N = N;
     p.BH = bh;
     p.n_qblocks = static_cast<int>(n_qblocks);
+    p.n_tiles = static_cast<int>(n_qblocks * BH);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
     cudaError_t e;
     const bool bf = dtype == FA_BF16;
-#define FA_LAUNCH(DD, BB, CC) e = launch<DD, BB, CC>(mq, mk, mv, mo, p, stream)
+#define FA_LAUNCH(DD, BB, CC) e = launch<DD, BB, CC>(mq, mk, mv, p, stream)
     if (D == 64) {
         if (bf) { if (causal) FA_LAUNCH(64, true, true); else FA_LAUNCH(64, true, false); }
         else    { if (causal) FA_LAUNCH(64, false, true); else FA_LAUNCH(64, false, false); }

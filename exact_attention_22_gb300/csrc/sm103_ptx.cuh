@@ -44,6 +44,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of three barrier phases at once (bit i set: phase i
+// complete); the three tests are in flight together.
+__device__ __forceinline__ uint32_t mbar_test3(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1, uint64_t* b2,
+                                               uint32_t p2) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred q0, q1, q2;\n\t.reg .b32 r0, r1, r2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+        "selp.b32 r0, 1, 0, q0;\n\t"
+        "selp.b32 r1, 2, 0, q1;\n\t"
+        "selp.b32 r2, 4, 0, q2;\n\t"
+        "or.b32 r0, r0, r1;\n\t"
+        "or.b32 %0, r0, r2;\n\t}"
+        : "=r"(r)
+        : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2)
+        : "memory");
+    return r;
+}
 // Wait for the phase of `bar` with the given parity to complete, giving up
 // after `timeout_ns` nanoseconds of wall time.  Returns false on time-out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
@@ -145,6 +165,31 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Same two forms with descriptor = base + immediate offset (in 16-byte units),
+// added inside the statement so only the base descriptor stays live.
+template <uint32_t OFF_A, uint32_t OFF_B>
+__device__ __forceinline__ void umma_ss_off(uint32_t d_tmem, uint64_t a_base, uint64_t b_base, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+        "add.s64 a, %1, %5;\n\t"
+        "add.s64 b, %2, %6;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_A), "n"(OFF_B)
+        : "memory");
+}
+template <uint32_t OFF_B>
+__device__ __forceinline__ void umma_ts_off(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_base, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\t"
+        "add.s64 b, %2, %5;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_B)
         : "memory");
 }
 // Arrive once on `bar` when every previously issued tcgen05.mma of this
