@@ -46,6 +46,8 @@ def load_library():
         lib.fa_fwd.restype = I
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = I
+        lib.fa_selftest_wait_timeout.argtypes = [vp]
+        lib.fa_selftest_wait_timeout.restype = I
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -61,6 +63,11 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, D: 
 
 def fa_get_device_status(stream: int) -> int:
     return int(load_library().fa_get_device_status(stream))
+
+
+def fa_selftest_wait_timeout(stream: int) -> int:
+    """Queue the bounded-wait self-test kernel (see include/fa.h)."""
+    return int(load_library().fa_selftest_wait_timeout(stream))
 
 
 def fa_status_string(status: int) -> str:

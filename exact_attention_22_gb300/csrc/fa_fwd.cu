@@ -59,6 +59,7 @@ enum : unsigned {
     ST_CORRECTION = 8u,
     ST_DRAIN = 16u,
     ST_Q_PRODUCER = 32u,
+    ST_SELFTEST = 64u,
 };
 
 constexpr int kTileM = 128;     // query rows of one Q tile (UMMA M)
@@ -702,6 +703,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// One warp waits, with the forward kernel's own bounded wait, on an mbarrier
+// that nothing arrives on: the wait gives up after its time limit, records a
+// status bit and the kernel returns normally.
+__global__ void __launch_bounds__(32) selftest_wait_timeout_kernel() {
+    __shared__ SharedState sh;
+    if (threadIdx.x == 0) {
+        mbar_init(&sh.drain, 1);
+        sh.abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const bool ok = __all_sync(0xffffffffu, wait_bar(&sh.drain, 0, &sh.abort_flag));
+    if (!ok && threadIdx.x == 0) give_up(sh, ST_SELFTEST);
+}
+
 // ------------------------------------------------------------------ host
 
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -825,6 +841,11 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
     }
 #undef FA_LAUNCH
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" int fa_selftest_wait_timeout(cudaStream_t stream) {
+    selftest_wait_timeout_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 extern "C" int fa_get_device_status(cudaStream_t stream) {

@@ -70,6 +70,16 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  */
 int fa_get_device_status(cudaStream_t stream);
 
+/*
+ * fa_selftest_wait_timeout -- diagnostic of the library's failure path (the
+ * pages have no counterpart).  Queues on `stream` a one-warp kernel whose only
+ * mbarrier wait can never complete; the wait gives up after the same 1 s limit
+ * every wait of fa_fwd has, records its status bit and the kernel returns.
+ * A following fa_get_device_status(stream) then reports FA_ERR_TIMEOUT, and
+ * the CUDA context stays usable.  No fault or hang is involved.
+ */
+int fa_selftest_wait_timeout(cudaStream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* fa_status_string(int status);
 

@@ -169,3 +169,20 @@ def test_bad_arguments_leave_outputs_untouched():
     torch.cuda.synchronize()
     assert (o == 7).all() and (lse == 7).all()
     assert fa.fa_get_device_status(0) == fa.FA_OK
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    """A wait that nothing completes gives up after its limit and is reported
+    as FA_ERR_TIMEOUT; the next forward pass on the same context is correct."""
+    import time
+    s = torch.cuda.Stream()
+    t0 = time.time()
+    assert fa.fa_selftest_wait_timeout(s.cuda_stream) == fa.FA_OK
+    assert fa.fa_get_device_status(s.cuda_stream) == 5          # FA_ERR_TIMEOUT
+    assert 0.5 < time.time() - t0 < 30
+    assert fa.fa_get_device_status(s.cuda_stream) == fa.FA_OK   # reading clears it
+    w = fa_inputs.Workload("after", 1, 2, 300, 64, True, "fp16")
+    q, k, v = fa_inputs.make_qkv(w, seed=9)
+    o, lse = _run(q, k, v, True, w.scale)
+    o_ref, lse_ref = _oracle_full(q, k, v, True, w.scale)
+    _check(o, lse, o_ref, lse_ref, "fp16", what="after self-test")
