@@ -326,3 +326,86 @@ int fa_ref_blocked(const void* q, const void* k, const void* v, int enc,
     if (visited) *visited = pairs_head0;
     return failed ? -2 : 0;
 }
+
+/* ---- split along the keys, then merge ----------------------------------- */
+
+int fa_ref_split_merge(const void* q, const void* k, const void* v, int enc,
+                       double* o, double* lse,
+                       long B, long H, long N, long D, double scale, int causal,
+                       long chunk, double* part_m, double* part_l, long part_cap,
+                       int nthreads)
+{
+    if (bad_args(q, k, v, enc, B, H, N, D) || !o || !lse || chunk < 1) return -1;
+    set_threads(nthreads);
+    long rows = B * H * N;
+    long nchunks = (N + chunk - 1) / chunk;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* pm = (double*)malloc(sizeof(double) * (size_t)nchunks);
+        double* pl = (double*)malloc(sizeof(double) * (size_t)nchunks);
+        double* po = (double*)malloc(sizeof(double) * (size_t)nchunks * (size_t)D);
+        if (!pm || !pl || !po) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < rows; ++r) {
+            if (!pm || !pl || !po) continue;
+            long bh = r / N, i = r % N;
+            size_t head_base = (size_t)bh * (size_t)N * (size_t)D;
+            size_t qrow = head_base + (size_t)i * (size_t)D;
+            long nvis = causal ? (i + 1 < N ? i + 1 : N) : N;
+            /* the partial of each chunk, by the definition over its keys */
+            for (long c = 0; c < nchunks; ++c) {
+                long j0 = c * chunk, j1 = j0 + chunk < nvis ? j0 + chunk : nvis;
+                double* oc = po + (size_t)c * (size_t)D;
+                for (long d = 0; d < D; ++d) oc[d] = 0.0;
+                pm[c] = -INFINITY;
+                pl[c] = 0.0;
+                for (long j = j0; j < j1; ++j) {
+                    size_t krow = head_base + (size_t)j * (size_t)D;
+                    double dot = 0.0;
+                    for (long d = 0; d < D; ++d) dot += load(q, enc, qrow + d) * load(k, enc, krow + d);
+                    if (scale * dot > pm[c]) pm[c] = scale * dot;
+                }
+                for (long j = j0; j < j1; ++j) {
+                    size_t krow = head_base + (size_t)j * (size_t)D;
+                    size_t vrow = head_base + (size_t)j * (size_t)D;
+                    double dot = 0.0;
+                    for (long d = 0; d < D; ++d) dot += load(q, enc, qrow + d) * load(k, enc, krow + d);
+                    double p = exp(scale * dot - pm[c]);
+                    pl[c] += p;
+                    for (long d = 0; d < D; ++d) oc[d] += p * load(v, enc, vrow + d);
+                }
+            }
+            if (r == 0 && part_m && part_l) {
+                for (long c = 0; c < nchunks && c < part_cap; ++c) {
+                    part_m[c] = pm[c];
+                    part_l[c] = pl[c];
+                }
+            }
+            /* the merge */
+            double m = -INFINITY;
+            for (long c = 0; c < nchunks; ++c)
+                if (pl[c] > 0.0 && pm[c] > m) m = pm[c];
+            double l = 0.0;
+            double* orow = o + (size_t)r * (size_t)D;
+            for (long d = 0; d < D; ++d) orow[d] = 0.0;
+            for (long c = 0; c < nchunks; ++c) {
+                if (!(pl[c] > 0.0)) continue;
+                double w = exp(pm[c] - m);
+                l += w * pl[c];
+                for (long d = 0; d < D; ++d) orow[d] += w * po[(size_t)c * (size_t)D + d];
+            }
+            if (l > 0.0) {
+                for (long d = 0; d < D; ++d) orow[d] /= l;
+                lse[r] = m + log(l);
+            } else {
+                lse[r] = -INFINITY;
+            }
+        }
+        free(pm); free(pl); free(po);
+    }
+    return failed ? -2 : 0;
+}

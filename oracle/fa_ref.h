@@ -77,6 +77,23 @@ int fa_ref_blocked(const void* q, const void* k, const void* v, int enc,
                    long trace_row, double* trace, long trace_cap, long* trace_len,
                    long* visited, int nthreads);
 
+/* Split along the keys, then merge ("CUDA FlashAttention: from online softmax
+ * to the long-sequence IO limit", section 7: several workers each produce a
+ * local (m, l, o) for a contiguous range of keys; the partials are reduced
+ * with the same merge formula as the online recurrence).  For every row the
+ * keys are cut into chunks of `chunk` keys; chunk s gives, over its visible
+ * keys, m_s = max score, l_s = sum exp(s - m_s), o_s = sum exp(s - m_s) v
+ * (a chunk with no visible key gives m_s = -inf, l_s = 0); then
+ *     m = max_s m_s,  l = sum_s exp(m_s - m) l_s,
+ *     O = sum_s exp(m_s - m) o_s / l,  LSE = m + ln l.
+ * If part_m / part_l are not NULL they receive the partials of row 0 of head 0
+ * (at most part_cap chunks, in chunk order). */
+int fa_ref_split_merge(const void* q, const void* k, const void* v, int enc,
+                       double* o, double* lse,
+                       long B, long H, long N, long D, double scale, int causal,
+                       long chunk, double* part_m, double* part_l, long part_cap,
+                       int nthreads);
+
 /* Threads the OpenMP runtime would use for nthreads <= 0. */
 int fa_ref_max_threads(void);
 

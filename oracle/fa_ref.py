@@ -55,6 +55,8 @@ def _load():
         lib.fa_ref_blocked.argtypes = [vp, vp, vp, I, dp, dp, L, L, L, L, Dbl, I, L, L, I, I,
                                        L, dp, L, lp, lp, I]
         lib.fa_ref_blocked.restype = I
+        lib.fa_ref_split_merge.argtypes = [vp, vp, vp, I, dp, dp, L, L, L, L, Dbl, I, L, dp, dp, L, I]
+        lib.fa_ref_split_merge.restype = I
         lib.fa_ref_max_threads.argtypes = []
         lib.fa_ref_max_threads.restype = I
         _lib = lib
@@ -150,3 +152,24 @@ def blocked(q, k, v, scale, causal=False, Br=64, Bc=64, kv_outer=False, rescale=
     if rc != 0:
         raise RuntimeError("fa_ref_blocked failed (%d)" % rc)
     return o, lse, (tr[: tlen.value].copy() if tr is not None else None), int(vis.value)
+
+
+def split_merge(q, k, v, scale, causal=False, chunk=128, enc="f64", nthreads=0, parts=0):
+    """Keys cut into chunks of `chunk`, partial (m, l, o) per chunk, merged.
+
+    Returns (O, LSE) or, with parts > 0, (O, LSE, m_parts, l_parts) where the
+    partials are those of row 0 of head 0.
+    """
+    q, k, v = _prep(q, k, v, enc)
+    B, H, N, D = q.shape
+    o = np.empty((B, H, N, D), np.float64)
+    lse = np.empty((B, H, N), np.float64)
+    pm = np.zeros(max(parts, 1), np.float64)
+    pl = np.zeros(max(parts, 1), np.float64)
+    rc = _load().fa_ref_split_merge(q.ctypes.data, k.ctypes.data, v.ctypes.data, ENC[enc], _dptr(o), _dptr(lse),
+                                    B, H, N, D, float(scale), int(bool(causal)), int(chunk),
+                                    _dptr(pm) if parts else None, _dptr(pl) if parts else None, int(parts),
+                                    int(nthreads))
+    if rc != 0:
+        raise RuntimeError("fa_ref_split_merge failed (%d)" % rc)
+    return (o, lse, pm[:parts], pl[:parts]) if parts else (o, lse)

@@ -223,3 +223,34 @@ def test_rows_entry_matches_full():
     orow, lrow = fa_ref.naive_rows(Q, K, V, 0.25, True, bh, rows)
     assert np.array_equal(orow, o.reshape(B * H, N, D)[bh, rows])
     assert np.array_equal(lrow, lse.reshape(B * H, N)[bh, rows])
+
+
+def test_split_merge_worked_row():
+    """mpbf.cn/news/61284, section 2.2, as two workers: chunk [1,2] has local
+    max 2 and sum 1.368, chunk [3,4] local max 4 and sum 1.368; merged at max 4
+    the sum is 1.368 * e^-2 + 1.368 = 1.553 (the split-K reduction of the CUDA
+    FlashAttention page, section 7, uses the same merge)."""
+    g = kv("worked_row_split.txt")
+    scores = [float(x) for x in g["scores"].split()]
+    N = len(scores)
+    q = np.zeros((N, 1)); q[0, 0] = 1.0
+    k = np.array(scores).reshape(N, 1)
+    v = np.ones((N, 1))
+    _, lse, pm, pl = fa_ref.split_merge(q, k, v, 1.0, chunk=int(g["block_split"]), parts=2)
+    dec = int(g["printed_decimals"])
+    assert list(pm) == [2.0, 4.0]
+    assert round(pl[0], dec) == float(g["block1_sum"]) and round(pl[1], dec) == float(g["block1_sum"])
+    merged = pl[0] * math.exp(pm[0] - pm[1]) + pl[1]
+    assert round(merged, dec) == float(g["block2_sum"])
+    assert abs(lse[0, 0, 0] - (4.0 + math.log(merged))) < 1e-15
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("chunk", [1, 7, 64, 128, 1000])
+def test_split_merge_equals_naive(causal, chunk):
+    """The merged result is the exact attention: it equals the naive form to
+    rounding, for any chunk size, including chunks past every visible key."""
+    Q, K, V = _normal(77, 300, 32)
+    ref, lref = fa_ref.naive(Q, K, V, 0.2, causal)
+    got, lgot = fa_ref.split_merge(Q, K, V, 0.2, causal, chunk=chunk)
+    assert np.abs(ref - got).max() < 1e-12 and np.abs(lref - lgot).max() < 1e-12
