@@ -46,6 +46,10 @@ def load_library():
         lib.fa_fwd.restype = I
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = I
+        lib.fa_splitkv_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, I, I, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_splitkv.restype = I
         lib.fa_selftest_wait_timeout.argtypes = [vp]
         lib.fa_selftest_wait_timeout.restype = I
         lib.fa_status_string.argtypes = [I]
@@ -61,6 +65,18 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, D: 
                                      stream))
 
 
+def fa_splitkv_workspace_bytes(B: int, H: int, N: int, D: int, num_splits: int) -> int:
+    return int(load_library().fa_splitkv_workspace_bytes(B, H, N, D, num_splits))
+
+
+def fa_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, D: int, scale: float,
+                   causal: int, dtype: int, num_splits: int, workspace: int, workspace_bytes: int,
+                   stream: int) -> int:
+    """Direct call of the split-K entry point; returns its status code."""
+    return int(load_library().fa_fwd_splitkv(q, k, v, o, lse, B, H, N, D, float(scale), int(causal), int(dtype),
+                                             int(num_splits), workspace, int(workspace_bytes), stream))
+
+
 def fa_get_device_status(stream: int) -> int:
     return int(load_library().fa_get_device_status(stream))
 
@@ -74,11 +90,14 @@ def fa_status_string(status: int) -> str:
     return load_library().fa_status_string(int(status)).decode()
 
 
-def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
+              num_splits: int = 0, workspace=None):
     """O, LSE = attention(Q, K, V) for contiguous [B,H,N,D] fp16/bf16 CUDA tensors.
 
     Outputs are allocated with torch when not given.  Raises FaError on a
     non-OK status.  Asynchronous on ``stream`` (default: torch's current stream).
+    ``num_splits`` > 0 selects the split-K path (fa_fwd_splitkv); its workspace
+    is allocated with torch unless one is given.
     """
     import torch
 
@@ -101,8 +120,19 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    dt = FA_BF16 if q.dtype == torch.bfloat16 else FA_FP16
+    if num_splits > 0:
+        need = fa_splitkv_workspace_bytes(B, H, N, D, num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        st = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D,
+                            scale, int(bool(causal)), dt, num_splits, workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), handle)
+        if st != FA_OK:
+            raise FaError(st, "fa_fwd_splitkv")
+        return out, lse
     st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D, scale,
-                int(bool(causal)), FA_BF16 if q.dtype == torch.bfloat16 else FA_FP16, handle)
+                int(bool(causal)), dt, handle)
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
     return out, lse

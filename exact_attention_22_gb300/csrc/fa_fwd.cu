@@ -103,35 +103,53 @@ struct __align__(8) SharedState {
 struct Params {
     void* o;
     float* lse;
+    float* ws_o;         // split mode: partial O, [splits][BH][N][D] fp32 (null otherwise)
+    float4* ws_st;       // split mode: partial (m, l, l_exact, -), [splits][BH][N]
     int N;
     int BH;
     int n_qblocks;       // ceil(N / 256)
-    int n_tiles;         // n_qblocks * BH
+    int n_splits;        // chunks of K/V tiles per query block (1 without a split)
+    int n_tiles;         // n_qblocks * BH * n_splits
     float scale_log2;    // scale * log2(e)
 };
 
-// One work tile: query rows q0 .. q0+255 of head bh.
+// One work tile: query rows q0 .. q0+255 of head bh, K/V tiles j0 .. j0+n_all-1
+// (chunk `split` of the query block's range).
 struct Tile {
-    int q0, bh, n_all;
-    int nkv[kNumQ];      // K/V tiles each stream visits (0: stream starts past N)
+    int q0, bh, split, j0, n_all;
+    int nkv[kNumQ];      // K/V tiles of this chunk each stream visits (0: none)
+    int last[kNumQ];     // global index of each stream's last K/V tile (its causal diagonal)
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool SPLIT>
 __device__ __forceinline__ Tile make_tile(const Params& p, int idx) {
     Tile w;
     // heaviest query block first: causal work grows with the block index
-    w.q0 = (p.n_qblocks - 1 - idx / p.BH) * kRowsPerTile;
-    w.bh = idx % p.BH;
-    w.n_all = 0;
+    const int qbh = SPLIT ? idx / p.n_splits : idx;
+    w.split = SPLIT ? idx - qbh * p.n_splits : 0;
+    w.q0 = (p.n_qblocks - 1 - qbh / p.BH) * kRowsPerTile;
+    w.bh = qbh % p.BH;
+    int full[kNumQ], full_all = 0;
 #pragma unroll
     for (int t = 0; t < kNumQ; ++t) {
         const int r0 = w.q0 + kTileM * t;
         if (r0 >= p.N)
-            w.nkv[t] = 0;
+            full[t] = 0;
         else if (CAUSAL)
-            w.nkv[t] = min(r0 + kTileM - 1, p.N - 1) / kTileN + 1;
+            full[t] = min(r0 + kTileM - 1, p.N - 1) / kTileN + 1;
         else
-            w.nkv[t] = (p.N + kTileN - 1) / kTileN;
+            full[t] = (p.N + kTileN - 1) / kTileN;
+        full_all = max(full_all, full[t]);
+    }
+    // chunk `split` of the query block's K/V range [0, full_all)
+    const int chunk = SPLIT ? (full_all + p.n_splits - 1) / p.n_splits : full_all;
+    w.j0 = SPLIT ? min(w.split * chunk, full_all) : 0;
+    const int j1 = SPLIT ? min(w.j0 + chunk, full_all) : full_all;
+    w.n_all = 0;
+#pragma unroll
+    for (int t = 0; t < kNumQ; ++t) {
+        w.nkv[t] = max(0, min(j1, full[t]) - w.j0);
+        w.last[t] = full[t] - 1;
         w.n_all = max(w.n_all, w.nkv[t]);
     }
     return w;
@@ -217,7 +235,7 @@ __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, float (&s)[128])
 // ------------------------------------------------------------------ roles
 
 // K/V producer: one thread; K_j then V_j of every work tile, in order.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                 const Params& p) {
     using C = Cfg<D>;
@@ -230,7 +248,7 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
     for (int k = 0; ok; ++k) {
         const int idx = tile_index(k, p.n_tiles);
         if (idx < 0) break;
-        const Tile w = make_tile<CAUSAL>(p, idx);
+        const Tile w = make_tile<CAUSAL, SPLIT>(p, idx);
         for (int j = 0; j < w.n_all && ok; ++j) {
 #pragma unroll 1
             for (int kind = 0; kind < 2; ++kind, ++item) {   // K_j, then V_j
@@ -244,7 +262,7 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
                 const CUtensorMap* map = kind ? tm_v : tm_k;
                 for (int b = 0; b < C::kBoxes; ++b)
                     tma_load_3d_hint(tiles + C::kOffKV + slot * C::kTileBytes + b * C::kBoxBytes, map,
-                                     &sh.kv_full[slot], 64 * b, j * kTileN, w.bh, pol_keep);
+                                     &sh.kv_full[slot], 64 * b, (w.j0 + j) * kTileN, w.bh, pol_keep);
             }
         }
     }
@@ -258,7 +276,7 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
 }
 
 // Q producer: one thread; Q_t of every work tile once its buffer is free.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 __device__ void run_q_producer(SharedState& sh, uint8_t* tiles, const CUtensorMap* tm_q, const Params& p) {
     using C = Cfg<D>;
     volatile int* abort_flag = &sh.abort_flag;
@@ -269,7 +287,7 @@ __device__ void run_q_producer(SharedState& sh, uint8_t* tiles, const CUtensorMa
     for (int k = 0; ok; ++k) {
         const int idx = tile_index(k, p.n_tiles);
         if (idx < 0) break;
-        const Tile w = make_tile<CAUSAL>(p, idx);
+        const Tile w = make_tile<CAUSAL, SPLIT>(p, idx);
         for (int t = 0; t < kNumQ; ++t) {
             if (w.nkv[t] == 0) continue;
             if (!wait_bar(&sh.q_empty[t], (loads[t] & 1) ^ 1, abort_flag)) {
@@ -294,10 +312,14 @@ __device__ void run_q_producer(SharedState& sh, uint8_t* tiles, const CUtensorMa
 // UMMA issuer: one thread.
 //
 // Ring items are K_0, V_0, K_1, V_1, ... of each work tile in turn; they are
-// acquired (full barrier waited) in that order.  An item is released (empty
-// barrier committed after the MMA that reads it) by the last stream that
-// reads it: stream 1, or stream 0 where stream 1 does not visit that K/V tile.
-template <int D, bool BF16, bool CAUSAL>
+// acquired (full barrier waited) in that order.  An item is released (its
+// slot's empty barrier committed after the MMA that reads it) by the last
+// MMA issued that reads it.  Within a round stream 0 goes first, so that is
+// stream 1 where it reads the item, else stream 0.  The one exception is a
+// work tile's K_0: a stream's first S of the next tile goes out early, at the
+// end of its previous tile, and stream 0 may start only at the top of the tile
+// (when it had no K/V tiles in the previous one), after stream 1.
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Params& p) {
     using C = Cfg<D>;
     volatile int* abort_flag = &sh.abort_flag;
@@ -357,12 +379,13 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
         umma_commit(&sh.pv_done[t]);
         if (release) umma_commit(&sh.kv_empty[item % C::kStages]);
     };
-    // First S of stream t in work tile w (ring items from `base`).
-    auto start_stream = [&](int t, const Tile& w, int base) -> bool {
+    // First S of stream t in work tile w (ring items from `base`); it releases
+    // K_0 unless the other stream reads it and has not issued its first S yet.
+    auto start_stream = [&](int t, const Tile& w, int base, bool other_done) -> bool {
         if (!wait_bar(&sh.q_full[t], (q_par >> t) & 1, abort_flag)) return false;
         q_par ^= 1u << t;
         if (!acquire(base)) return false;
-        issue_s(t, base, t == kNumQ - 1 || w.nkv[kNumQ - 1] == 0);
+        issue_s(t, base, w.nkv[kNumQ - 1 - t] == 0 || other_done);
         if (w.nkv[t] == 1) umma_commit(&sh.q_empty[t]);   // that was its last S of this work tile
         return true;
     };
@@ -370,17 +393,19 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
     int k = 0;
     int idx = tile_index(0, p.n_tiles);
     if (idx < 0) return;
-    Tile cur = make_tile<CAUSAL>(p, idx);
+    Tile cur = make_tile<CAUSAL, SPLIT>(p, idx);
     int cur_base = 0;
     uint32_t started = 0;    // bit t: first S of `cur` already issued by the previous tile
     while (ok) {
         const int nidx = tile_index(k + 1, p.n_tiles);
         const bool has_next = nidx >= 0;
-        const Tile nxt = has_next ? make_tile<CAUSAL>(p, nidx) : cur;
+        const Tile nxt = has_next ? make_tile<CAUSAL, SPLIT>(p, nidx) : cur;
         const int nxt_base = cur_base + 2 * cur.n_all;
-#pragma unroll
-        for (int t = 0; t < kNumQ; ++t)
-            if (ok && cur.nkv[t] > 0 && !((started >> t) & 1)) ok = start_stream(t, cur, cur_base);
+        if (ok && cur.nkv[0] > 0 && !(started & 1u)) {
+            ok = start_stream(0, cur, cur_base, (started & 2u) != 0);
+            started |= 1u;
+        }
+        if (ok && cur.nkv[1] > 0 && !(started & 2u)) ok = start_stream(1, cur, cur_base, true);
         uint32_t nstarted = 0;
         for (int j = 0; j < cur.n_all && ok; ++j) {
 #pragma unroll
@@ -413,7 +438,7 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
                     issue_s(t, item_k, t == kNumQ - 1 || j + 1 >= cur.nkv[kNumQ - 1]);
                     if (j + 2 == cur.nkv[t]) umma_commit(&sh.q_empty[t]);
                 } else if (has_next && nxt.nkv[t] > 0) {
-                    ok = start_stream(t, nxt, nxt_base);
+                    ok = start_stream(t, nxt, nxt_base, ((nstarted >> (kNumQ - 1 - t)) & 1u) != 0);
                     nstarted |= 1u << t;
                 }
             }
@@ -431,7 +456,7 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
     if (!wait_bar(&sh.drain, 0, &never)) atomicOr(&g_fa_status, ST_DRAIN);
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params& p) {
     volatile int* abort_flag = &sh.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -447,10 +472,16 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
     for (int k = 0; ok; ++k) {
         const int idx = tile_index(k, p.n_tiles);
         if (idx < 0) break;
-        const Tile w = make_tile<CAUSAL>(p, idx);
+        const Tile w = make_tile<CAUSAL, SPLIT>(p, idx);
         const int nkv_t = w.nkv[t];
-        if (nkv_t == 0) continue;
         const int qi = w.q0 + kTileM * t + r;                 // global query index of this row
+        const size_t row_g = static_cast<size_t>(w.bh) * N + qi;
+        if (nkv_t == 0) {
+            // split mode: this chunk holds none of the stream's keys
+            if (SPLIT && qi < N)
+                p.ws_st[static_cast<size_t>(w.split) * p.BH * N + row_g] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+            continue;
+        }
 
         float m_ref = -INFINITY;   // reference max, log2 units of the scaled score
         float l = 0.f;             // running sum of the 16-bit-rounded P actually used by P V
@@ -462,8 +493,9 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             float s[kTileN];
             tmem_ld128_wait(ts, s);
 
-            const int k0 = j * kTileN;
-            const bool need_mask = (CAUSAL && j == nkv_t - 1) || (k0 + kTileN > N);
+            const int jg = SPLIT ? w.j0 + j : j;                // global K/V tile index
+            const int k0 = jg * kTileN;
+            const bool need_mask = (CAUSAL && jg == (SPLIT ? w.last[t] : nkv_t - 1)) || (k0 + kTileN > N);
             if (need_mask) {
 #pragma unroll
                 for (int c = 0; c < kTileN; ++c) {
@@ -566,10 +598,28 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
         ok = __all_sync(0xffffffffu, wait_bar(&sh.pv_done[t], (step - 1) & 1, abort_flag));
         if (!ok) break;
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
         const bool row_ok = qi < N;
-        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                               (static_cast<size_t>(w.bh) * N + (row_ok ? qi : 0)) * D);
+        if constexpr (SPLIT) {
+            // split mode: the unnormalised partial and its (m, l) go to the workspace
+            const size_t prow = static_cast<size_t>(w.split) * p.BH * N + row_g;
+            float4* dst = reinterpret_cast<float4*>(p.ws_o + prow * D);
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                uint32_t v[32];
+                tmem_ld32_wait(to + c, v);
+                if (row_ok) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        dst[c / 4 + q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                     __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                }
+            }
+            if (row_ok) p.ws_st[prow] = make_float4(m_ref, l, ls, 0.f);
+            tc_fence_before();
+            continue;
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + (row_ok ? row_g : 0) * D);
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
             uint32_t v[32];
@@ -587,7 +637,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             }
         }
         if (row_ok)
-            p.lse[static_cast<size_t>(w.bh) * N + qi] =
+            p.lse[row_g] =
                 ls > 0.f ? (m_ref + log2f(ls)) * 0.69314718055994531f : -INFINITY;
         // The next work tile's first P V overwrites O_t; it waits for this
         // stream's next p_full, which comes after these loads.
@@ -596,7 +646,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
     if (!ok) give_up(sh, ST_SOFTMAX);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 __device__ void run_correction(SharedState& sh, uint32_t tmem, const Params& p) {
     using C = Cfg<D>;
     volatile int* abort_flag = &sh.abort_flag;
@@ -608,7 +658,7 @@ __device__ void run_correction(SharedState& sh, uint32_t tmem, const Params& p) 
     for (int k = 0; ok; ++k) {
         const int idx = tile_index(k, p.n_tiles);
         if (idx < 0) break;
-        const Tile w = make_tile<CAUSAL>(p, idx);
+        const Tile w = make_tile<CAUSAL, SPLIT>(p, idx);
         for (int j = 0; j < w.n_all && ok; ++j) {
             for (int t = 0; t < kNumQ; ++t) {
                 if (j >= w.nkv[t]) continue;
@@ -643,7 +693,7 @@ __device__ void run_correction(SharedState& sh, uint32_t tmem, const Params& p) 
     if (!ok) give_up(sh, ST_CORRECTION);
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -681,18 +731,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (wg == 0) {
         setmaxnreg_dec<96>();
         if (warp == 0 && lane == 0)
-            run_kv_producer<D, CAUSAL>(sh, tiles, &tm_k, &tm_v, p);
+            run_kv_producer<D, CAUSAL, SPLIT>(sh, tiles, &tm_k, &tm_v, p);
         else if (warp == 1 && lane == 0)
-            run_mma<D, BF16, CAUSAL>(sh, tiles, tmem, p);
+            run_mma<D, BF16, CAUSAL, SPLIT>(sh, tiles, tmem, p);
         else if (warp == 2 && lane == 0)
-            run_q_producer<D, CAUSAL>(sh, tiles, &tm_q, p);
+            run_q_producer<D, CAUSAL, SPLIT>(sh, tiles, &tm_q, p);
         __syncwarp();
     } else if (wg <= kNumQ) {
         setmaxnreg_inc<176>();
-        run_softmax<D, BF16, CAUSAL>(sh, tmem, wg - 1, p);
+        run_softmax<D, BF16, CAUSAL, SPLIT>(sh, tmem, wg - 1, p);
     } else {
         setmaxnreg_dec<64>();
-        run_correction<D, CAUSAL>(sh, tmem, p);
+        run_correction<D, CAUSAL, SPLIT>(sh, tmem, p);
     }
 
     tc_fence_before();
@@ -701,6 +751,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+// Merge of the split partials, one warp per query row (HBM-bound):
+//   m = max_s m_s,  w_s = 2^(m_s - m),  O = sum_s w_s O_s / sum_s w_s l_s,
+//   LSE = (m + log2 sum_s w_s l_exact_s) * ln 2,
+// skipping partials with l_s = 0 (chunks without a visible key).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__ ws_o,
+                                                       const float4* __restrict__ ws_st, void* o, float* lse,
+                                                       long long rows, int n_splits) {
+    constexpr int kPer = D / 32;   // elements of the row per lane
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    float m = -INFINITY;
+    for (int s = 0; s < n_splits; ++s) {
+        const float4 st = ws_st[static_cast<size_t>(s) * rows + row];
+        if (st.y > 0.f) m = fmaxf(m, st.x);
+    }
+    float wsum = 0.f, lsum = 0.f, acc[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+    for (int s = 0; s < n_splits; ++s) {
+        const float4 st = ws_st[static_cast<size_t>(s) * rows + row];
+        if (!(st.y > 0.f)) continue;
+        const float wgt = exp2f(st.x - m);
+        wsum += wgt * st.y;
+        lsum += wgt * st.z;
+        const float* src = ws_o + (static_cast<size_t>(s) * rows + row) * D + lane * kPer;
+        if constexpr (kPer == 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src);
+            acc[0] += wgt * x.x; acc[1] += wgt * x.y; acc[2] += wgt * x.z; acc[3] += wgt * x.w;
+        } else {
+            const float2 x = *reinterpret_cast<const float2*>(src);
+            acc[0] += wgt * x.x; acc[1] += wgt * x.y;
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint32_t pk[kPer / 2];
+#pragma unroll
+    for (int i = 0; i < kPer / 2; ++i)
+        pk[i] = BF16 ? pack_bf16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv) : pack_f16x2(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    uint16_t* orow = static_cast<uint16_t*>(o) + static_cast<size_t>(row) * D + lane * kPer;
+    if constexpr (kPer == 4)
+        *reinterpret_cast<uint2*>(orow) = make_uint2(pk[0], pk[1]);
+    else
+        *reinterpret_cast<uint32_t*>(orow) = pk[0];
+    if (lane == 0) lse[row] = lsum > 0.f ? (m + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
 }
 
 // One warp waits, with the forward kernel's own bounded wait, on an mbarrier
@@ -763,10 +861,10 @@ static int sm_count(int dev) {
     return n;
 }
 
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
                           cudaStream_t stream) {
-    auto kern = fa_fwd_kernel<D, BF16, CAUSAL>;
+    auto kern = fa_fwd_kernel<D, BF16, CAUSAL, SPLIT>;
     static std::atomic<uint64_t> configured{0};   // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -793,8 +891,11 @@ static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 using namespace fa103;
 
-extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
-                      float scale, int causal, int dtype, cudaStream_t stream) {
+namespace fa103 {
+
+// Argument checks and kernel parameters shared by both forward entry points.
+static int prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+                   float scale, int causal, int dtype, int n_splits, CUtensorMap (&maps)[3], Params& p) {
     if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
@@ -807,31 +908,35 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
     const uint64_t elems = BH * static_cast<uint64_t>(N) * static_cast<uint64_t>(D);
     if (BH > 0x7fffffffull || elems >= (uint64_t(1) << 40)) return FA_ERR_INVALID_ARG;
     const uint64_t n_qblocks = (static_cast<uint64_t>(N) + kRowsPerTile - 1) / kRowsPerTile;
-    if (n_qblocks * BH > 0x7fffffffull) return FA_ERR_INVALID_ARG;
+    if (n_qblocks * BH * static_cast<uint64_t>(n_splits) > 0x7fffffffull) return FA_ERR_INVALID_ARG;
     const size_t tbytes = static_cast<size_t>(elems) * 2, lbytes = static_cast<size_t>(BH) * N * sizeof(float);
     const void* ins[3] = {q, k, v};
     for (const void* in : ins)
         if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes)) return FA_ERR_INVALID_ARG;
     if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
 
-    CUtensorMap mq, mk, mv;
     const int bh = static_cast<int>(BH);
-    if (!make_tile_map(&mq, q, dtype, D, N, bh) || !make_tile_map(&mk, k, dtype, D, N, bh) ||
-        !make_tile_map(&mv, v, dtype, D, N, bh))
+    if (!make_tile_map(&maps[0], q, dtype, D, N, bh) || !make_tile_map(&maps[1], k, dtype, D, N, bh) ||
+        !make_tile_map(&maps[2], v, dtype, D, N, bh))
         return FA_ERR_CUDA;
-
-    Params p;
     p.o = o;
     p.lse = lse;
+    p.ws_o = nullptr;
+    p.ws_st = nullptr;
     p.N = N;
     p.BH = bh;
     p.n_qblocks = static_cast<int>(n_qblocks);
-    p.n_tiles = static_cast<int>(n_qblocks * BH);
+    p.n_splits = n_splits;
+    p.n_tiles = static_cast<int>(n_qblocks * BH * static_cast<uint64_t>(n_splits));
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    return FA_OK;
+}
 
+template <bool SPLIT>
+static int dispatch(const CUtensorMap (&m)[3], const Params& p, int D, int dtype, int causal, cudaStream_t stream) {
     cudaError_t e;
     const bool bf = dtype == FA_BF16;
-#define FA_LAUNCH(DD, BB, CC) e = launch<DD, BB, CC>(mq, mk, mv, p, stream)
+#define FA_LAUNCH(DD, BB, CC) e = launch<DD, BB, CC, SPLIT>(m[0], m[1], m[2], p, stream)
     if (D == 64) {
         if (bf) { if (causal) FA_LAUNCH(64, true, true); else FA_LAUNCH(64, true, false); }
         else    { if (causal) FA_LAUNCH(64, false, true); else FA_LAUNCH(64, false, false); }
@@ -841,6 +946,70 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
     }
 #undef FA_LAUNCH
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+static int dispatch_merge(const Params& p, int D, int dtype, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(p.BH) * p.N;
+    const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+    const bool bf = dtype == FA_BF16;
+    if (D == 64) {
+        if (bf) fa_merge_kernel<64, true><<<grid, 256, 0, stream>>>(p.ws_o, p.ws_st, p.o, p.lse, rows, p.n_splits);
+        else    fa_merge_kernel<64, false><<<grid, 256, 0, stream>>>(p.ws_o, p.ws_st, p.o, p.lse, rows, p.n_splits);
+    } else {
+        if (bf) fa_merge_kernel<128, true><<<grid, 256, 0, stream>>>(p.ws_o, p.ws_st, p.o, p.lse, rows, p.n_splits);
+        else    fa_merge_kernel<128, false><<<grid, 256, 0, stream>>>(p.ws_o, p.ws_st, p.o, p.lse, rows, p.n_splits);
+    }
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+constexpr int kMaxSplits = 64;
+
+static size_t splitkv_bytes(long long rows, int D, int n_splits) {
+    return static_cast<size_t>(n_splits) * static_cast<size_t>(rows) * (static_cast<size_t>(D) * 4 + 16);
+}
+
+}  // namespace fa103
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
+                      float scale, int causal, int dtype, cudaStream_t stream) {
+    CUtensorMap maps[3];
+    Params p;
+    const int st = prepare(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, 1, maps, p);
+    if (st != FA_OK) return st;
+    return dispatch<false>(maps, p, D, dtype, causal, stream);
+}
+
+extern "C" size_t fa_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits) {
+    if (B < 1 || H < 1 || N < 1 || (D != 64 && D != 128) || num_splits < 1 || num_splits > kMaxSplits) return 0;
+    return splitkv_bytes(static_cast<long long>(B) * H * N, D, num_splits);
+}
+
+extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                              int N, int D, float scale, int causal, int dtype, int num_splits, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+    if (num_splits < 1 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+    const size_t need = fa_splitkv_workspace_bytes(B, H, N, D, num_splits);
+    if (need != 0) {   // sizes valid: check the workspace before anything touches CUDA
+        if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return FA_ERR_MISALIGNED;
+        if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+        const long long rows0 = static_cast<long long>(B) * H * N;
+        const size_t tbytes = static_cast<size_t>(rows0) * D * 2, lbytes = static_cast<size_t>(rows0) * 4;
+        const void* others[4] = {q, k, v, o};
+        for (const void* x : others)
+            if (x != nullptr && overlaps(workspace, need, x, tbytes)) return FA_ERR_INVALID_ARG;
+        if (lse != nullptr && overlaps(workspace, need, lse, lbytes)) return FA_ERR_INVALID_ARG;
+    }
+    CUtensorMap maps[3];
+    Params p;
+    int st = prepare(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, num_splits, maps, p);
+    if (st != FA_OK) return st;
+    const long long rows = static_cast<long long>(p.BH) * N;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_st = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) +
+                                        static_cast<size_t>(num_splits) * rows * D * 4);
+    st = dispatch<true>(maps, p, D, dtype, causal, stream);
+    if (st != FA_OK) return st;
+    return dispatch_merge(p, D, dtype, stream);
 }
 
 extern "C" int fa_selftest_wait_timeout(cudaStream_t stream) {

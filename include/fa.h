@@ -24,6 +24,7 @@
 #define FA_GB300_FA_H
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -60,6 +61,38 @@ typedef enum {
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int D, float scale, int causal, int dtype,
            cudaStream_t stream);
+
+/*
+ * fa_splitkv_workspace_bytes -- bytes of workspace fa_fwd_splitkv needs for
+ * these sizes: num_splits * B*H*N * (4*D + 16).  Returns 0 for invalid sizes
+ * (any size < 1, D not 64 or 128, num_splits > 64).
+ */
+size_t fa_splitkv_workspace_bytes(int B, int H, int N, int D, int num_splits);
+
+/*
+ * fa_fwd_splitkv -- the same forward pass, with the key/value range of each
+ * 256-row query block cut into `num_splits` contiguous chunks that different
+ * CTAs process ("CUDA FlashAttention: from online softmax to the long-sequence
+ * IO limit", section 7: for long N and small B*H, split along the keys, let
+ * each worker produce a local (m, l, o) and reduce them with the same merge
+ * formula).  Each chunk writes its unnormalised partial O (fp32) and its
+ * running max and sums to `workspace`; a second kernel, queued on the same
+ * stream, merges them into o and lse.
+ *
+ *   num_splits  1 .. 64 (1 still goes through the workspace and the merge)
+ *   workspace   DEVICE memory owned by the caller, 16-byte aligned, at least
+ *               fa_splitkv_workspace_bytes(B, H, N, D, num_splits) bytes;
+ *               overwritten, contents undefined afterwards; must not overlap
+ *               q, k, v, o or lse
+ *
+ * All other arguments, layouts and errors are those of fa_fwd; a workspace
+ * that is too small returns FA_ERR_INVALID_ARG, a null or misaligned one
+ * FA_ERR_MISALIGNED.  Calls that share a workspace must not overlap in time.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                   int B, int H, int N, int D, float scale, int causal, int dtype,
+                   int num_splits, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
 
 /*
  * fa_get_device_status -- synchronise `stream`, then report whether any

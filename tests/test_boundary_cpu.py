@@ -74,3 +74,21 @@ def test_binding_rejects_cpu_tensors(lib):
     x = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
     with pytest.raises(ValueError):
         fa.attention(x, x, x)
+
+
+def test_splitkv_workspace_size(lib):
+    assert fa.fa_splitkv_workspace_bytes(2, 3, 100, 128, 5) == 5 * 2 * 3 * 100 * (4 * 128 + 16)
+    for bad in ((0, 1, 1, 64, 1), (1, 1, 1, 96, 1), (1, 1, 1, 64, 0), (1, 1, 1, 64, 65)):
+        assert fa.fa_splitkv_workspace_bytes(*bad) == 0
+
+
+@pytest.mark.parametrize("splits,ws,ws_bytes,status", [
+    (0, 6 << 20, 1 << 20, 1), (65, 6 << 20, 1 << 20, 1),
+    (4, 6 << 20, 16, 1),                     # too small
+    (4, 0, 1 << 20, 3), (4, (6 << 20) + 4, 1 << 20, 3),
+    (4, (4 << 20) - 1024, 1 << 20, 1),       # overlaps o
+])
+def test_splitkv_argument_errors_without_gpu(lib, splits, ws, ws_bytes, status):
+    a = GOOD
+    assert fa.fa_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"], a["scale"],
+                             a["causal"], a["dtype"], splits, ws, ws_bytes, 0) == status
