@@ -18,7 +18,7 @@ _LIB_PATH = os.path.join(_PKG, "libfa.so")
 FA_FP16, FA_BF16 = 0, 1
 FA_OK = 0
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
-                4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+                4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT", 6: "FA_ERR_TOO_LARGE"}
 
 _lib = None
 
@@ -50,6 +50,10 @@ def load_library():
         lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, I, I, vp, ctypes.c_size_t, vp]
         lib.fa_fwd_splitkv.restype = I
+        lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, I, I, vp]
+        lib.fa_fwd_splitkv_noalloc.restype = I
+        lib.fa_noalloc_scratch_bytes.argtypes = []
+        lib.fa_noalloc_scratch_bytes.restype = ctypes.c_size_t
         lib.fa_selftest_wait_timeout.argtypes = [vp]
         lib.fa_selftest_wait_timeout.restype = I
         lib.fa_status_string.argtypes = [I]
@@ -75,6 +79,18 @@ def fa_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: 
     """Direct call of the split-K entry point; returns its status code."""
     return int(load_library().fa_fwd_splitkv(q, k, v, o, lse, B, H, N, D, float(scale), int(causal), int(dtype),
                                              int(num_splits), workspace, int(workspace_bytes), stream))
+
+
+def fa_fwd_splitkv_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, D: int,
+                           scale: float, causal: int, dtype: int, num_splits: int, stream: int) -> int:
+    """Split-K forward for callers that cannot allocate device memory: the
+    workspace is the library's fixed scratch buffer (see include/fa.h)."""
+    return int(load_library().fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, N, D, float(scale), int(causal),
+                                                     int(dtype), int(num_splits), stream))
+
+
+def fa_noalloc_scratch_bytes() -> int:
+    return int(load_library().fa_noalloc_scratch_bytes())
 
 
 def fa_get_device_status(stream: int) -> int:

@@ -1012,6 +1012,58 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
     return dispatch_merge(p, D, dtype, stream);
 }
 
+// ------------------------------------------------------------------ no-allocation split-K
+//
+// Some callers cannot allocate device memory around this call: a host
+// framework that owns every device allocation and hands the library only its
+// tensors, or a latency-critical loop in which cudaMalloc / cudaFree (which can
+// synchronise the whole device) are not allowed.  For them the split-K pass can
+// use a scratch buffer that lives in this library for the life of the process:
+// a fixed array in device memory, reserved on every GPU that loads the library.
+namespace fa103 {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;   // 64 MiB per device
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device.  In host code the array's name is only a stand-in for the
+// symbol, so the kernels must be given this address, never the name.
+static int noalloc_scratch(void** out) {
+    static std::atomic<void*> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev >= 0 && dev < 64) {
+        void* p = cache[dev].load();
+        if (p != nullptr) {
+            *out = p;
+            return FA_OK;
+        }
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
+    if (dev >= 0 && dev < 64) cache[dev].store(p);
+    *out = p;
+    return FA_OK;
+}
+
+}  // namespace fa103
+
+extern "C" size_t fa_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+extern "C" int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                      int H, int N, int D, float scale, int causal, int dtype, int num_splits,
+                                      cudaStream_t stream) {
+    if (num_splits < 1 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+    // Invalid sizes give 0 here and are reported by fa_fwd_splitkv below.
+    if (fa_splitkv_workspace_bytes(B, H, N, D, num_splits) > kNoAllocScratchBytes) return FA_ERR_TOO_LARGE;
+    void* scratch = nullptr;
+    const int st = noalloc_scratch(&scratch);
+    if (st != FA_OK) return st;
+    return fa_fwd_splitkv(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, num_splits, scratch,
+                          kNoAllocScratchBytes, stream);
+}
+
 extern "C" int fa_selftest_wait_timeout(cudaStream_t stream) {
     selftest_wait_timeout_kernel<<<1, 32, 0, stream>>>();
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -1037,6 +1089,7 @@ extern "C" const char* fa_status_string(int status) {
         case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
         case FA_ERR_CUDA: return "FA_ERR_CUDA";
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+        case FA_ERR_TOO_LARGE: return "FA_ERR_TOO_LARGE";
         default: return "FA_ERR_UNKNOWN";
     }
 }

@@ -38,7 +38,9 @@ typedef enum {
     FA_ERR_UNSUPPORTED = 2,   /* head dimension other than 64 or 128           */
     FA_ERR_MISALIGNED = 3,    /* null pointer or not 16-byte aligned           */
     FA_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed          */
-    FA_ERR_TIMEOUT = 5        /* a bounded in-kernel wait gave up (see below)  */
+    FA_ERR_TIMEOUT = 5,       /* a bounded in-kernel wait gave up (see below)  */
+    FA_ERR_TOO_LARGE = 6      /* the problem does not fit the fixed scratch of
+                                 fa_fwd_splitkv_noalloc                        */
 } fa_status;
 
 /*
@@ -93,6 +95,41 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    int B, int H, int N, int D, float scale, int causal, int dtype,
                    int num_splits, void* workspace, size_t workspace_bytes,
                    cudaStream_t stream);
+
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this entry point exists for
+ * the library's users, not for the method.
+ *
+ * Who needs it: code that may not call cudaMalloc / cudaFree around this call,
+ * e.g. a host framework that owns every device allocation and passes the
+ * library only its tensors, or a latency-critical loop where an allocation,
+ * which can synchronise the whole device, is not acceptable.  Instead of a
+ * caller-provided workspace it uses a scratch buffer of
+ * fa_noalloc_scratch_bytes() bytes (64 MiB) held in the library's own device
+ * memory; every GPU that loads the library keeps that buffer until the process
+ * exits.  The caller still provides q, k, v, o and lse, as for fa_fwd.
+ *
+ * Limits and behaviour:
+ *   - returns FA_ERR_TOO_LARGE, without launching anything, when
+ *     fa_splitkv_workspace_bytes(B, H, N, D, num_splits) exceeds the scratch
+ *     size (use fewer splits, or fa_fwd_splitkv with your own workspace);
+ *   - no allocation of any kind is made: the first call on a device looks up
+ *     the buffer's device address (once per device, with that device current);
+ *     make that first call before any stream capture on that device;
+ *   - all calls on a device share the one buffer; calls that may overlap on
+ *     the GPU (different streams without ordering between them) race and give
+ *     wrong results.  Nothing needs clearing between calls: each call writes
+ *     every part of the buffer it later reads;
+ *   - all other arguments, layouts and status codes are those of
+ *     fa_fwd_splitkv.
+ */
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int D, float scale, int causal, int dtype,
+                           int num_splits, cudaStream_t stream);
+
+/* Size in bytes of the scratch buffer fa_fwd_splitkv_noalloc uses. */
+size_t fa_noalloc_scratch_bytes(void);
 
 /*
  * fa_get_device_status -- synchronise `stream`, then report whether any
