@@ -256,9 +256,20 @@ def run_ours(args, w):
     handle = stream.cuda_stream
     dt = fa.FA_BF16 if w.dtype == "bf16" else fa.FA_FP16
 
+    splits = args.num_splits
+    ws = ws_bytes = None
+    if splits > 0:
+        ws_bytes = fa.fa_splitkv_workspace_bytes(w.B, w.H, w.N, w.D, splits)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
     def launch(qq, kk, vv, oo, ll):
-        st = fa.fa_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(), ll.data_ptr(), w.B, w.H, w.N,
-                       w.D, w.scale, int(w.causal), dt, handle)
+        if splits > 0:
+            st = fa.fa_fwd_splitkv(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(), ll.data_ptr(), w.B,
+                                   w.H, w.N, w.D, w.scale, int(w.causal), dt, splits, ws.data_ptr(), ws_bytes,
+                                   handle)
+        else:
+            st = fa.fa_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(), ll.data_ptr(), w.B, w.H,
+                           w.N, w.D, w.scale, int(w.causal), dt, handle)
         if st != fa.FA_OK:
             raise fa.FaError(st, "fa_fwd")
 
@@ -282,7 +293,7 @@ def run_ours(args, w):
             ends[i].record(stream)
         torch.cuda.synchronize()
         barrier()
-    launches = args.steps
+    launches = args.steps * (2 if splits > 0 else 1)   # split-K: forward + merge kernel
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
     status = fa.fa_get_device_status(handle)
@@ -330,7 +341,8 @@ def run_ours(args, w):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
                    "scale": w.scale, "parallelism": "replica per GPU" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (256 MiB write, outside the events)",
-                   "ms_p50": statistics.median(step_ms), "ms_min": min(step_ms)},
+                   "ms_p50": statistics.median(step_ms), "ms_min": min(step_ms),
+                   "num_splits": splits, "entry": "fa_fwd_splitkv" if splits > 0 else "fa_fwd"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(w.name),
                      "peak_kind": "%s dense bf16 (burst); fp16/bf16 nominal ratio 1" % peak_kind,
@@ -364,6 +376,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-splits", type=int, default=0,
+                    help="time fa_fwd_splitkv with this many K/V chunks per query block (0: fa_fwd)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -63,6 +63,9 @@ WORKLOADS = {
     "ragged_causal_bf16_b1h8n32749d128": Workload("ragged_causal_bf16_b1h8n32749d128", 1, 8, 32749, 128,
                                                   True, "bf16"),
 }
+# One long head: too few query blocks to fill the GPU, where splitting the keys pays.
+WORKLOADS["longhead_causal_bf16_b1h1n32768d128"] = Workload("longhead_causal_bf16_b1h1n32768d128", 1, 1, 32768, 128,
+                                                             True, "bf16")
 for _n in (512, 1024, 2048, 4096, 8192):
     _w = Workload("causal_fp16_b1h32n%dd128" % _n, 1, 32, _n, 128, True, "fp16")
     WORKLOADS[_w.name] = _w

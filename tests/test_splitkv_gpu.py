@@ -88,3 +88,16 @@ def test_splitkv_causal_many_short_chunks(splits):
                                        rows, enc="f16")
     idx = (torch.from_numpy(bh).cuda(), torch.from_numpy(rows).cuda())
     _check(o.reshape(32, w.N, w.D)[idx], lse.reshape(32, w.N)[idx], o_ref, lse_ref, "fp16", what="S=%d" % splits)
+
+
+def test_splitkv_single_long_head_sampled_rows():
+    """The regime split-K is for: one head, N = 32768, causal."""
+    w = fa_inputs.WORKLOADS["longhead_causal_bf16_b1h1n32768d128"]
+    q, k, v = fa_inputs.make_qkv(w, seed=0)
+    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=True, num_splits=4)
+    torch.cuda.synchronize()
+    bh, rows = _sample_rows(w)
+    o_ref, lse_ref = fa_ref.naive_rows(fa_inputs.bits(q), fa_inputs.bits(k), fa_inputs.bits(v), w.scale, True, bh,
+                                       rows, enc="bf16")
+    idx = (torch.from_numpy(bh).cuda(), torch.from_numpy(rows).cuda())
+    _check(o.reshape(1, w.N, w.D)[idx], lse.reshape(1, w.N)[idx], o_ref, lse_ref, "bf16", what="split long head")
