@@ -107,11 +107,11 @@ static void set_threads(int nthreads)
  * s is scratch of length N. */
 static void naive_row(const void* q, const void* k, const void* v, int enc,
                       long N, long D, double scale, int causal,
-                      size_t head_base, long i, double* s,
+                      size_t q_base, size_t head_base, long i, double* s,
                       double* o_row, double* lse_out)
 {
     long nvis = causal ? (i + 1 < N ? i + 1 : N) : N;
-    size_t qrow = head_base + (size_t)i * (size_t)D;
+    size_t qrow = q_base + (size_t)i * (size_t)D;
     for (long d = 0; d < D; ++d) o_row[d] = 0.0;
     if (nvis <= 0) {
         *lse_out = -INFINITY;
@@ -159,7 +159,7 @@ int fa_ref_naive(const void* q, const void* k, const void* v, int enc,
             if (!s) continue;
             long bh = r / N, i = r % N;
             size_t head_base = (size_t)bh * (size_t)N * (size_t)D;
-            naive_row(q, k, v, enc, N, D, scale, causal, head_base, i, s,
+            naive_row(q, k, v, enc, N, D, scale, causal, head_base, head_base, i, s,
                       o + (size_t)r * (size_t)D, lse + r);
         }
         free(s);
@@ -189,7 +189,7 @@ int fa_ref_naive_rows(const void* q, const void* k, const void* v, int enc,
         for (long r = 0; r < nrows; ++r) {
             if (!s) continue;
             size_t head_base = (size_t)bh_idx[r] * (size_t)N * (size_t)D;
-            naive_row(q, k, v, enc, N, D, scale, causal, head_base, row_idx[r], s,
+            naive_row(q, k, v, enc, N, D, scale, causal, head_base, head_base, row_idx[r], s,
                       o_rows + (size_t)r * (size_t)D, lse_rows + r);
         }
         free(s);
@@ -406,6 +406,41 @@ int fa_ref_split_merge(const void* q, const void* k, const void* v, int enc,
             }
         }
         free(pm); free(pl); free(po);
+    }
+    return failed ? -2 : 0;
+}
+
+/* ---- grouped key/value heads ------------------------------------------- */
+
+int fa_ref_naive_gqa(const void* q, const void* k, const void* v, int enc,
+                     double* o, double* lse,
+                     long B, long H, long H_kv, long N, long D, double scale, int causal,
+                     int nthreads)
+{
+    if (bad_args(q, k, v, enc, B, H, N, D) || !o || !lse) return -1;
+    if (H_kv < 1 || H % H_kv != 0) return -1;
+    set_threads(nthreads);
+    long rows = B * H * N;
+    long group = H / H_kv;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!s) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 16)
+        for (long r = 0; r < rows; ++r) {
+            if (!s) continue;
+            long bh = r / N, i = r % N;
+            long b = bh / H, h = bh % H;
+            size_t q_base = (size_t)bh * (size_t)N * (size_t)D;
+            size_t kv_base = ((size_t)b * (size_t)H_kv + (size_t)(h / group)) * (size_t)N * (size_t)D;
+            naive_row(q, k, v, enc, N, D, scale, causal, q_base, kv_base, i, s,
+                      o + (size_t)r * (size_t)D, lse + r);
+        }
+        free(s);
     }
     return failed ? -2 : 0;
 }

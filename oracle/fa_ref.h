@@ -94,6 +94,16 @@ int fa_ref_split_merge(const void* q, const void* k, const void* v, int enc,
                        long chunk, double* part_m, double* part_l, long part_cap,
                        int nthreads);
 
+/* Grouped key/value heads ("CUDA FlashAttention: from online softmax to the
+ * long-sequence IO limit", section 7: GQA/MQA maps query heads onto shared
+ * K/V heads without copying K/V).  q is [B, H, N, D]; k and v are
+ * [B, H_kv, N, D] with H a multiple of H_kv; query head h reads K/V head
+ * h / (H / H_kv).  Otherwise the naive definition above. */
+int fa_ref_naive_gqa(const void* q, const void* k, const void* v, int enc,
+                     double* o, double* lse,
+                     long B, long H, long H_kv, long N, long D, double scale, int causal,
+                     int nthreads);
+
 /* Threads the OpenMP runtime would use for nthreads <= 0. */
 int fa_ref_max_threads(void);
 

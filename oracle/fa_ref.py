@@ -57,6 +57,8 @@ def _load():
         lib.fa_ref_blocked.restype = I
         lib.fa_ref_split_merge.argtypes = [vp, vp, vp, I, dp, dp, L, L, L, L, Dbl, I, L, dp, dp, L, I]
         lib.fa_ref_split_merge.restype = I
+        lib.fa_ref_naive_gqa.argtypes = [vp, vp, vp, I, dp, dp, L, L, L, L, L, Dbl, I, I]
+        lib.fa_ref_naive_gqa.restype = I
         lib.fa_ref_max_threads.argtypes = []
         lib.fa_ref_max_threads.restype = I
         _lib = lib
@@ -173,3 +175,24 @@ def split_merge(q, k, v, scale, causal=False, chunk=128, enc="f64", nthreads=0, 
     if rc != 0:
         raise RuntimeError("fa_ref_split_merge failed (%d)" % rc)
     return (o, lse, pm[:parts], pl[:parts]) if parts else (o, lse)
+
+
+def naive_gqa(q, k, v, scale, causal=False, enc="f64", nthreads=0):
+    """Safe-softmax attention with grouped K/V heads: q [B,H,N,D], k/v
+    [B,H_kv,N,D]; returns (O [B,H,N,D], LSE [B,H,N])."""
+    want = np.float64 if enc == "f64" else np.uint16
+    q, k, v = (np.ascontiguousarray(t) for t in (q, k, v))
+    for t in (q, k, v):
+        if t.dtype != want or t.ndim != 4:
+            raise TypeError("enc=%s needs 4-D %s arrays" % (enc, np.dtype(want)))
+    B, H, N, D = q.shape
+    H_kv = k.shape[1]
+    if k.shape != (B, H_kv, N, D) or v.shape != k.shape:
+        raise ValueError("k, v must be [B, H_kv, N, D]")
+    o = np.empty((B, H, N, D), np.float64)
+    lse = np.empty((B, H, N), np.float64)
+    rc = _load().fa_ref_naive_gqa(q.ctypes.data, k.ctypes.data, v.ctypes.data, ENC[enc], _dptr(o), _dptr(lse),
+                                  B, H, H_kv, N, D, float(scale), int(bool(causal)), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("fa_ref_naive_gqa failed (%d)" % rc)
+    return o, lse

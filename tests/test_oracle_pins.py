@@ -254,3 +254,29 @@ def test_split_merge_equals_naive(causal, chunk):
     ref, lref = fa_ref.naive(Q, K, V, 0.2, causal)
     got, lgot = fa_ref.split_merge(Q, K, V, 0.2, causal, chunk=chunk)
     assert np.abs(ref - got).max() < 1e-12 and np.abs(lref - lgot).max() < 1e-12
+
+
+@pytest.mark.parametrize("H,H_kv", [(8, 8), (8, 2), (6, 3), (4, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_equals_attention_on_repeated_kv(H, H_kv, causal):
+    """Grouped K/V heads are the same computation as copying each K/V head to
+    its H / H_kv query heads (CUDA FlashAttention page, section 7, describes
+    the mapping as a way to avoid that copy)."""
+    B, N, D = 2, 70, 16
+    rng = np.random.default_rng(H * 10 + H_kv)
+    q = rng.normal(size=(B, H, N, D)); k = rng.normal(size=(B, H_kv, N, D)); v = rng.normal(size=(B, H_kv, N, D))
+    o, lse = fa_ref.naive_gqa(q, k, v, 0.3, causal)
+    rep = H // H_kv
+    o2, lse2 = fa_ref.naive(q, np.repeat(k, rep, axis=1), np.repeat(v, rep, axis=1), 0.3, causal)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+def test_gqa_head_mapping_is_grouped_not_strided():
+    """Query head h reads K/V head h // (H / H_kv): give each K/V head a
+    constant value and read it back through uniform scores."""
+    B, H, H_kv, N, D = 1, 6, 2, 5, 4
+    q = np.zeros((B, H, N, D)); k = np.zeros((B, H_kv, N, D))
+    v = np.stack([np.full((N, D), float(g + 1)) for g in range(H_kv)])[None]
+    o, _ = fa_ref.naive_gqa(q, k, v, 1.0)
+    for h in range(H):
+        assert np.all(o[0, h] == h // (H // H_kv) + 1)
