@@ -46,6 +46,8 @@ def load_library():
         lib.fa_fwd.restype = I
         lib.fa_get_device_status.argtypes = [vp]
         lib.fa_get_device_status.restype = I
+        lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, F, I, I, vp]
+        lib.fa_fwd_gqa.restype = I
         lib.fa_splitkv_workspace_bytes.argtypes = [I, I, I, I, I]
         lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, I, I, vp, ctypes.c_size_t, vp]
@@ -67,6 +69,13 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, D: 
     """Direct call of the C entry point; returns its status code."""
     return int(load_library().fa_fwd(q, k, v, o, lse, B, H, N, D, float(scale), int(causal), int(dtype),
                                      stream))
+
+
+def fa_fwd_gqa(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, H_kv: int, N: int, D: int, scale: float,
+               causal: int, dtype: int, stream: int) -> int:
+    """Direct call of the grouped-K/V-head entry point; returns its status code."""
+    return int(load_library().fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, D, float(scale), int(causal), int(dtype),
+                                         stream))
 
 
 def fa_splitkv_workspace_bytes(B: int, H: int, N: int, D: int, num_splits: int) -> int:
@@ -108,7 +117,8 @@ def fa_status_string(status: int) -> str:
 
 def attention(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
               num_splits: int = 0, workspace=None):
-    """O, LSE = attention(Q, K, V) for contiguous [B,H,N,D] fp16/bf16 CUDA tensors.
+    """O, LSE = attention(Q, K, V) for contiguous fp16/bf16 CUDA tensors, Q [B,H,N,D]
+    and K, V [B,H_kv,N,D] (H_kv = H, or a divisor of H for grouped K/V heads).
 
     Outputs are allocated with torch when not given.  Raises FaError on a
     non-OK status.  Asynchronous on ``stream`` (default: torch's current stream).
@@ -121,8 +131,11 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
         raise ValueError("q, k, v must be CUDA tensors")
     if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("q, k, v must share one dtype, float16 or bfloat16")
-    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must all be [B, H, N, D]")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or k.shape[0] != q.shape[0] or k.shape[2:] != q.shape[2:]:
+        raise ValueError("q must be [B, H, N, D] and k, v [B, H_kv, N, D]")
+    if q.shape[1] % k.shape[1] != 0:
+        raise ValueError("the query heads H must be a multiple of the K/V heads H_kv")
+    H_kv = k.shape[1]
     for t in (q, k, v):
         if not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous")
@@ -146,6 +159,14 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
                             workspace.numel() * workspace.element_size(), handle)
         if st != FA_OK:
             raise FaError(st, "fa_fwd_splitkv")
+        return out, lse
+    if H_kv != H:
+        if num_splits > 0:
+            raise ValueError("split-K with grouped K/V heads is not provided")
+        st = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, H_kv, N, D,
+                        scale, int(bool(causal)), dt, handle)
+        if st != FA_OK:
+            raise FaError(st, "fa_fwd_gqa")
         return out, lse
     st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D, scale,
                 int(bool(causal)), dt, handle)

@@ -107,6 +107,8 @@ struct Params {
     float4* ws_st;       // split mode: partial (m, l, l_exact, -), [splits][BH][N]
     int N;
     int BH;
+    int H;               // query heads per batch entry
+    int kv_group;        // query heads per K/V head (1 without grouped K/V heads)
     int n_qblocks;       // ceil(N / 256)
     int n_splits;        // chunks of K/V tiles per query block (1 without a split)
     int n_tiles;         // n_qblocks * BH * n_splits
@@ -116,7 +118,7 @@ struct Params {
 // One work tile: query rows q0 .. q0+255 of head bh, K/V tiles j0 .. j0+n_all-1
 // (chunk `split` of the query block's range).
 struct Tile {
-    int q0, bh, split, j0, n_all;
+    int q0, bh, kvh, split, j0, n_all;   // kvh: K/V plane b * H_kv + h / kv_group
     int nkv[kNumQ];      // K/V tiles of this chunk each stream visits (0: none)
     int last[kNumQ];     // global index of each stream's last K/V tile (its causal diagonal)
 };
@@ -129,6 +131,7 @@ __device__ __forceinline__ Tile make_tile(const Params& p, int idx) {
     w.split = SPLIT ? idx - qbh * p.n_splits : 0;
     w.q0 = (p.n_qblocks - 1 - qbh / p.BH) * kRowsPerTile;
     w.bh = qbh % p.BH;
+    w.kvh = p.kv_group == 1 ? w.bh : (w.bh / p.H) * (p.H / p.kv_group) + (w.bh % p.H) / p.kv_group;
     int full[kNumQ], full_all = 0;
 #pragma unroll
     for (int t = 0; t < kNumQ; ++t) {
@@ -262,7 +265,7 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
                 const CUtensorMap* map = kind ? tm_v : tm_k;
                 for (int b = 0; b < C::kBoxes; ++b)
                     tma_load_3d_hint(tiles + C::kOffKV + slot * C::kTileBytes + b * C::kBoxBytes, map,
-                                     &sh.kv_full[slot], 64 * b, (w.j0 + j) * kTileN, w.bh, pol_keep);
+                                     &sh.kv_full[slot], 64 * b, (w.j0 + j) * kTileN, w.kvh, pol_keep);
             }
         }
     }
@@ -894,9 +897,10 @@ using namespace fa103;
 namespace fa103 {
 
 // Argument checks and kernel parameters shared by both forward entry points.
-static int prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int D,
-                   float scale, int causal, int dtype, int n_splits, CUtensorMap (&maps)[3], Params& p) {
+static int prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
+                   int D, float scale, int causal, int dtype, int n_splits, CUtensorMap (&maps)[3], Params& p) {
     if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
@@ -910,14 +914,17 @@ static int prepare(const void* q, const void* k, const void* v, void* o, float* 
     const uint64_t n_qblocks = (static_cast<uint64_t>(N) + kRowsPerTile - 1) / kRowsPerTile;
     if (n_qblocks * BH * static_cast<uint64_t>(n_splits) > 0x7fffffffull) return FA_ERR_INVALID_ARG;
     const size_t tbytes = static_cast<size_t>(elems) * 2, lbytes = static_cast<size_t>(BH) * N * sizeof(float);
+    const size_t kvbytes = tbytes / static_cast<size_t>(H / H_kv);
     const void* ins[3] = {q, k, v};
-    for (const void* in : ins)
-        if (overlaps(o, tbytes, in, tbytes) || overlaps(lse, lbytes, in, tbytes)) return FA_ERR_INVALID_ARG;
+    const size_t in_bytes[3] = {tbytes, kvbytes, kvbytes};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(o, tbytes, ins[i], in_bytes[i]) || overlaps(lse, lbytes, ins[i], in_bytes[i]))
+            return FA_ERR_INVALID_ARG;
     if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
 
-    const int bh = static_cast<int>(BH);
-    if (!make_tile_map(&maps[0], q, dtype, D, N, bh) || !make_tile_map(&maps[1], k, dtype, D, N, bh) ||
-        !make_tile_map(&maps[2], v, dtype, D, N, bh))
+    const int bh = static_cast<int>(BH), bhkv = B * H_kv;
+    if (!make_tile_map(&maps[0], q, dtype, D, N, bh) || !make_tile_map(&maps[1], k, dtype, D, N, bhkv) ||
+        !make_tile_map(&maps[2], v, dtype, D, N, bhkv))
         return FA_ERR_CUDA;
     p.o = o;
     p.lse = lse;
@@ -925,6 +932,8 @@ static int prepare(const void* q, const void* k, const void* v, void* o, float* 
     p.ws_st = nullptr;
     p.N = N;
     p.BH = bh;
+    p.H = H;
+    p.kv_group = H / H_kv;
     p.n_qblocks = static_cast<int>(n_qblocks);
     p.n_splits = n_splits;
     p.n_tiles = static_cast<int>(n_qblocks * BH * static_cast<uint64_t>(n_splits));
@@ -974,7 +983,16 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
                       float scale, int causal, int dtype, cudaStream_t stream) {
     CUtensorMap maps[3];
     Params p;
-    const int st = prepare(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, 1, maps, p);
+    const int st = prepare(q, k, v, o, lse, B, H, H, N, D, scale, causal, dtype, 1, maps, p);
+    if (st != FA_OK) return st;
+    return dispatch<false>(maps, p, D, dtype, causal, stream);
+}
+
+extern "C" int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
+                          int N, int D, float scale, int causal, int dtype, cudaStream_t stream) {
+    CUtensorMap maps[3];
+    Params p;
+    const int st = prepare(q, k, v, o, lse, B, H, H_kv, N, D, scale, causal, dtype, 1, maps, p);
     if (st != FA_OK) return st;
     return dispatch<false>(maps, p, D, dtype, causal, stream);
 }
@@ -1001,7 +1019,7 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
     }
     CUtensorMap maps[3];
     Params p;
-    int st = prepare(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, num_splits, maps, p);
+    int st = prepare(q, k, v, o, lse, B, H, H, N, D, scale, causal, dtype, num_splits, maps, p);
     if (st != FA_OK) return st;
     const long long rows = static_cast<long long>(p.BH) * N;
     p.ws_o = static_cast<float*>(workspace);

@@ -65,6 +65,25 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            cudaStream_t stream);
 
 /*
+ * fa_fwd_gqa -- the forward pass with grouped key/value heads (GQA; MQA when
+ * H_kv = 1): query head h of batch entry b reads K/V head h / (H / H_kv) of
+ * the same batch entry, without K/V being copied ("CUDA FlashAttention: from
+ * online softmax to the long-sequence IO limit", section 7, GQA/MQA).
+ *
+ *   q, o        [B, H, N, D]     (as for fa_fwd)
+ *   k, v        [B, H_kv, N, D]  (H_kv >= 1 and H a multiple of H_kv)
+ *   lse         [B, H, N] fp32
+ *
+ * Work tiles of query heads that share a K/V head run next to each other, so
+ * that K/V head is read from HBM about once and then from L2.  All other
+ * arguments, layouts and errors are those of fa_fwd; an H_kv that does not
+ * divide H returns FA_ERR_INVALID_ARG.  fa_fwd is fa_fwd_gqa with H_kv = H.
+ */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int H, int H_kv, int N, int D, float scale, int causal, int dtype,
+               cudaStream_t stream);
+
+/*
  * fa_splitkv_workspace_bytes -- bytes of workspace fa_fwd_splitkv needs for
  * these sizes: num_splits * B*H*N * (4*D + 16).  Returns 0 for invalid sizes
  * (any size < 1, D not 64 or 128, num_splits > 64).

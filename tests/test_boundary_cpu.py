@@ -92,3 +92,9 @@ def test_splitkv_argument_errors_without_gpu(lib, splits, ws, ws_bytes, status):
     a = GOOD
     assert fa.fa_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"], a["scale"],
                              a["causal"], a["dtype"], splits, ws, ws_bytes, 0) == status
+
+
+@pytest.mark.parametrize("H,H_kv,status", [(6, 4, 1), (6, 0, 1), (6, -2, 1), (4, 8, 1)])
+def test_gqa_head_count_errors(lib, H, H_kv, status):
+    a = GOOD
+    assert fa.fa_fwd_gqa(a["q"], a["k"], a["v"], a["o"], a["lse"], 1, H, H_kv, 256, 64, 0.125, 0, 0, 0) == status
