@@ -540,21 +540,22 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             // subtract after (then the largest element maps to exactly 2^0).
             const float msub = (m_ref == -INFINITY) ? 0.f : m_ref;
             const bool fused = fabsf(msub) < 16777216.f;
-            const uint64_t c2 = pack_f32x2(scale_log2, scale_log2);
+            if (!fused) {
+                // The product is rounded on its own first and the loop below only
+                // subtracts (coefficient 1).  One loop body serves both cases: a
+                // second unrolled copy of it costs instruction-cache misses.
+#pragma unroll
+                for (int c = 0; c < kTileN; ++c) s[c] = __fmul_rn(s[c], scale_log2);
+            }
+            const float cf = fused ? scale_log2 : 1.f;
+            const uint64_t c2 = pack_f32x2(cf, cf);
             const uint64_t nm2 = pack_f32x2(-msub, -msub);
             uint64_t lx2 = pack_f32x2(0.f, 0.f);   // sum of the fp32 p (bf16 only)
             uint32_t pk[kTileN / 2];                 // P as packed 16-bit pairs
 #pragma unroll
             for (int i = 0; i < kTileN / 2; ++i) {
                 float x0, x1;
-                if (fused) {
-                    const uint64_t s2 = pack_f32x2(s[2 * i], s[2 * i + 1]);
-                    unpack_f32x2(fma_f32x2(s2, c2, nm2), x0, x1);
-                } else {
-                    // never contracted into an fma: the product is rounded on its own
-                    x0 = __fadd_rn(__fmul_rn(s[2 * i], scale_log2), -msub);
-                    x1 = __fadd_rn(__fmul_rn(s[2 * i + 1], scale_log2), -msub);
-                }
+                unpack_f32x2(fma_f32x2(pack_f32x2(s[2 * i], s[2 * i + 1]), c2, nm2), x0, x1);
                 const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                 if constexpr (BF16) {
                     pk[i] = pack_bf16x2(p0, p1);
