@@ -17,7 +17,8 @@
 //     tile; tiles are dealt heaviest first, in a snake order over the CTAs;
 //   * TMA loads each Q tile once and streams K_j, V_j through a shared-memory
 //     ring (128-byte swizzle, mbarrier full/empty pairs);
-//   * one thread issues tcgen05 UMMAs: S_t = Q_t K_j^T into tensor memory
+//   * one warp issues tcgen05 UMMAs (all lanes run the control flow, one
+//     elected lane issues): S_t = Q_t K_j^T into tensor memory
 //     (TMEM), and O_t += P_t V_j with P_t read back from TMEM, where it
 //     overwrites the first half of S_t.  When a stream finishes its K/V tiles
 //     its next S is the first one of the CTA's next work tile, so the tensor
@@ -312,7 +313,15 @@ __device__ void run_q_producer(SharedState& sh, uint8_t* tiles, const CUtensorMa
     }
 }
 
-// UMMA issuer: one thread.
+__device__ __forceinline__ int lane_id() { return static_cast<int>(threadIdx.x & 31); }
+// Three barrier tests by lane 0, result broadcast so the warp stays uniform.
+__device__ __forceinline__ uint32_t mbar_test3_bcast(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1, uint64_t* b2,
+                                                     uint32_t p2) {
+    return __shfl_sync(0xffffffffu, mbar_test3(b0, p0, b1, p1, b2, p2), 0);
+}
+
+// UMMA issuer: warp 1.  All 32 lanes run the control flow below with the same
+// values, and each tcgen05.mma / tcgen05.commit is issued by one elected lane.
 //
 // Ring items are K_0, V_0, K_1, V_1, ... of each work tile in turn; they are
 // acquired (full barrier waited) in that order.  An item is released (its
@@ -343,7 +352,8 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
     auto acquire = [&](int it) -> bool {
         if (acquired > it) return true;
         do {
-            if (!wait_bar(&sh.kv_full[acquired % C::kStages], (acquired / C::kStages) & 1, abort_flag)) return false;
+            if (!__all_sync(0xffffffffu, wait_bar(&sh.kv_full[acquired % C::kStages], (acquired / C::kStages) & 1, abort_flag)))
+                return false;
         } while (++acquired <= it);
         tc_fence_after();
         return true;
@@ -353,43 +363,43 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
         const uint64_t db = dkv0 + (((item % C::kStages) * C::kTileBytes) >> 4);
         const uint32_t d = tmem + C::tm_s(t);
         // K-step kk reads 16 columns of D: 32 bytes into a 128-byte row, in box kk / 4
-        umma_ss_off<0, 0>(d, da, db, kIdS, 0);
-        umma_ss_off<2, 2>(d, da, db, kIdS, 1);
-        umma_ss_off<4, 4>(d, da, db, kIdS, 1);
-        umma_ss_off<6, 6>(d, da, db, kIdS, 1);
+        umma_ss_off_elect<0, 0>(d, da, db, kIdS, 0);
+        umma_ss_off_elect<2, 2>(d, da, db, kIdS, 1);
+        umma_ss_off_elect<4, 4>(d, da, db, kIdS, 1);
+        umma_ss_off_elect<6, 6>(d, da, db, kIdS, 1);
         if constexpr (D == 128) {
             constexpr uint32_t B = C::kBoxBytes >> 4;
-            umma_ss_off<B + 0, B + 0>(d, da, db, kIdS, 1);
-            umma_ss_off<B + 2, B + 2>(d, da, db, kIdS, 1);
-            umma_ss_off<B + 4, B + 4>(d, da, db, kIdS, 1);
-            umma_ss_off<B + 6, B + 6>(d, da, db, kIdS, 1);
+            umma_ss_off_elect<B + 0, B + 0>(d, da, db, kIdS, 1);
+            umma_ss_off_elect<B + 2, B + 2>(d, da, db, kIdS, 1);
+            umma_ss_off_elect<B + 4, B + 4>(d, da, db, kIdS, 1);
+            umma_ss_off_elect<B + 6, B + 6>(d, da, db, kIdS, 1);
         }
-        umma_commit(&sh.s_full[t]);
-        if (release) umma_commit(&sh.kv_empty[item % C::kStages]);
+        umma_commit_elect(&sh.s_full[t]);
+        if (release) umma_commit_elect(&sh.kv_empty[item % C::kStages]);
     };
     auto issue_pv = [&](int t, int item, bool first, bool release) {
         const uint64_t dv = dv0 + (((item % C::kStages) * C::kTileBytes) >> 4);
         const uint32_t d = tmem + C::tm_o(t), a = tmem + C::tm_s(t);
         // K-step kk reads 16 keys = 2048 bytes of V and 8 TMEM columns of P
-        umma_ts_off<0 * 128>(d, a + 0, dv, kIdO, first ? 0u : 1u);
-        umma_ts_off<1 * 128>(d, a + 8, dv, kIdO, 1);
-        umma_ts_off<2 * 128>(d, a + 16, dv, kIdO, 1);
-        umma_ts_off<3 * 128>(d, a + 24, dv, kIdO, 1);
-        umma_ts_off<4 * 128>(d, a + 32, dv, kIdO, 1);
-        umma_ts_off<5 * 128>(d, a + 40, dv, kIdO, 1);
-        umma_ts_off<6 * 128>(d, a + 48, dv, kIdO, 1);
-        umma_ts_off<7 * 128>(d, a + 56, dv, kIdO, 1);
-        umma_commit(&sh.pv_done[t]);
-        if (release) umma_commit(&sh.kv_empty[item % C::kStages]);
+        umma_ts_off_elect<0 * 128>(d, a + 0, dv, kIdO, first ? 0u : 1u);
+        umma_ts_off_elect<1 * 128>(d, a + 8, dv, kIdO, 1);
+        umma_ts_off_elect<2 * 128>(d, a + 16, dv, kIdO, 1);
+        umma_ts_off_elect<3 * 128>(d, a + 24, dv, kIdO, 1);
+        umma_ts_off_elect<4 * 128>(d, a + 32, dv, kIdO, 1);
+        umma_ts_off_elect<5 * 128>(d, a + 40, dv, kIdO, 1);
+        umma_ts_off_elect<6 * 128>(d, a + 48, dv, kIdO, 1);
+        umma_ts_off_elect<7 * 128>(d, a + 56, dv, kIdO, 1);
+        umma_commit_elect(&sh.pv_done[t]);
+        if (release) umma_commit_elect(&sh.kv_empty[item % C::kStages]);
     };
     // First S of stream t in work tile w (ring items from `base`); it releases
     // K_0 unless the other stream reads it and has not issued its first S yet.
     auto start_stream = [&](int t, const Tile& w, int base, bool other_done) -> bool {
-        if (!wait_bar(&sh.q_full[t], (q_par >> t) & 1, abort_flag)) return false;
+        if (!__all_sync(0xffffffffu, wait_bar(&sh.q_full[t], (q_par >> t) & 1, abort_flag))) return false;
         q_par ^= 1u << t;
         if (!acquire(base)) return false;
         issue_s(t, base, w.nkv[kNumQ - 1 - t] == 0 || other_done);
-        if (w.nkv[t] == 1) umma_commit(&sh.q_empty[t]);   // that was its last S of this work tile
+        if (w.nkv[t] == 1) umma_commit_elect(&sh.q_empty[t]);   // that was its last S of this work tile
         return true;
     };
 
@@ -421,15 +431,16 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
                 // that fails falls back to a bounded wait.
                 const int need = more ? item_v + 1 : item_v;
                 const int item_k = more ? item_v + 1 : item_v;
-                const uint32_t got = mbar_test3(&sh.kv_full[item_v % C::kStages], (item_v / C::kStages) & 1,
-                                                &sh.kv_full[item_k % C::kStages], (item_k / C::kStages) & 1,
-                                                &sh.p_full[t], (pv_par >> t) & 1);
+                const uint32_t got = mbar_test3_bcast(&sh.kv_full[item_v % C::kStages], (item_v / C::kStages) & 1,
+                                                      &sh.kv_full[item_k % C::kStages], (item_k / C::kStages) & 1,
+                                                      &sh.p_full[t], (pv_par >> t) & 1);
                 const bool r_p = (got & 4u) != 0;
                 if ((got & 3u) == 3u && acquired >= item_v && acquired <= need) {
                     acquired = need + 1;   // both tested complete above
                     tc_fence_after();
                 }
-                if (!acquire(need) || (!r_p && !wait_bar(&sh.p_full[t], (pv_par >> t) & 1, abort_flag))) {
+                if (!acquire(need) ||
+                    (!r_p && !__all_sync(0xffffffffu, wait_bar(&sh.p_full[t], (pv_par >> t) & 1, abort_flag)))) {
                     ok = false;
                     continue;
                 }
@@ -439,7 +450,7 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
                 if (more) {
                     const int item_k = item_v + 1;
                     issue_s(t, item_k, t == kNumQ - 1 || j + 1 >= cur.nkv[kNumQ - 1]);
-                    if (j + 2 == cur.nkv[t]) umma_commit(&sh.q_empty[t]);
+                    if (j + 2 == cur.nkv[t]) umma_commit_elect(&sh.q_empty[t]);
                 } else if (has_next && nxt.nkv[t] > 0) {
                     ok = start_stream(t, nxt, nxt_base, ((nstarted >> (kNumQ - 1 - t)) & 1u) != 0);
                     nstarted |= 1u << t;
@@ -452,11 +463,11 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
         cur_base = nxt_base;
         started = nstarted;
     }
-    if (!ok) give_up(sh, ST_MMA);
+    if (!ok && lane_id() == 0) give_up(sh, ST_MMA);
     // Nothing of ours may still be in flight when the CTA retires.
-    umma_commit(&sh.drain);
+    umma_commit_elect(&sh.drain);
     volatile int never = 0;
-    if (!wait_bar(&sh.drain, 0, &never)) atomicOr(&g_fa_status, ST_DRAIN);
+    if (!__all_sync(0xffffffffu, wait_bar(&sh.drain, 0, &never)) && lane_id() == 0) atomicOr(&g_fa_status, ST_DRAIN);
 }
 
 template <int D, bool BF16, bool CAUSAL, bool SPLIT>
@@ -736,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         setmaxnreg_dec<96>();
         if (warp == 0 && lane == 0)
             run_kv_producer<D, CAUSAL, SPLIT>(sh, tiles, &tm_k, &tm_v, p);
-        else if (warp == 1 && lane == 0)
+        else if (warp == 1)
             run_mma<D, BF16, CAUSAL, SPLIT>(sh, tiles, tmem, p);
         else if (warp == 2 && lane == 0)
             run_q_producer<D, CAUSAL, SPLIT>(sh, tiles, &tm_q, p);

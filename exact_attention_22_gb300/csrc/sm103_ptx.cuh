@@ -192,6 +192,43 @@ __device__ __forceinline__ void umma_ts_off(uint32_t d_tmem, uint32_t a_tmem, ui
         "r"(a_tmem), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_B)
         : "memory");
 }
+// The same two forms and the commit, issued by one lane that elect.sync picks
+// from a converged warp (the lowest active lane, the same one every time for a
+// full warp).  The whole warp runs the issuer's control flow, which then stays
+// warp-uniform: each issue is cheaper than from a lone lane of a divergent
+// branch.
+template <uint32_t OFF_A, uint32_t OFF_B>
+__device__ __forceinline__ void umma_ss_off_elect(uint32_t d_tmem, uint64_t a_base, uint64_t b_base, uint32_t idesc,
+                                                  uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 a, b;\n\t"
+        "add.s64 a, %1, %5;\n\t"
+        "add.s64 b, %2, %6;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_A), "n"(OFF_B)
+        : "memory");
+}
+template <uint32_t OFF_B>
+__device__ __forceinline__ void umma_ts_off_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_base, uint32_t idesc,
+                                                  uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 b;\n\t"
+        "add.s64 b, %2, %5;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_B)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
+}
 // Arrive once on `bar` when every previously issued tcgen05.mma of this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
