@@ -1,5 +1,6 @@
 /*
- * fa_ref.c -- FP64 CPU oracle for the exact attention forward pass.
+ * fa_ref.c -- FP64 CPU oracle for the exact attention forward and backward
+ * passes.
  *
  * TEST INFRASTRUCTURE ONLY (see fa_ref.h).  Plain loops in double precision,
  * no blocking beyond what the blocked form itself states, no fusion.
@@ -443,4 +444,212 @@ int fa_ref_naive_gqa(const void* q, const void* k, const void* v, int enc,
         free(s);
     }
     return failed ? -2 : 0;
+}
+
+/* ---- backward pass ------------------------------------------------------ */
+
+/* Row i of a head ("Why FlashAttention does not need to store the attention
+ * matrix", section 3.3; "CUDA FlashAttention: from online softmax to the
+ * long-sequence IO limit", section 4.3.1): the scores s_ij, the row's
+ * log-sum-exp, P_ij = exp(s_ij - LSE_i), dP_ij = dO_i . v_j, the softmax
+ * correction term Delta_i = rowsum(dP_i (x) P_i), and, if dq_row is given,
+ * dQ_i = scale * sum_j P_ij (dP_ij - Delta_i) k_j.  s and dp are scratch of
+ * length N.  A row without visible keys gives LSE = -inf, Delta = 0, dQ = 0. */
+static void bwd_row(const void* q, const void* k, const void* v, const void* dout, int enc,
+                    long N, long D, double scale, int causal, size_t q_base, size_t kv_base,
+                    long i, double* s, double* dp, double* lse_out, double* delta_out, double* dq_row)
+{
+    long nvis = causal ? (i + 1 < N ? i + 1 : N) : N;
+    size_t qrow = q_base + (size_t)i * (size_t)D;
+    if (dq_row)
+        for (long d = 0; d < D; ++d) dq_row[d] = 0.0;
+    if (nvis <= 0) {
+        *lse_out = -INFINITY;
+        *delta_out = 0.0;
+        return;
+    }
+    double m = -INFINITY;
+    for (long j = 0; j < nvis; ++j) {
+        size_t kvrow = kv_base + (size_t)j * (size_t)D;
+        double dot = 0.0, dpo = 0.0;
+        for (long d = 0; d < D; ++d) {
+            dot += load(q, enc, qrow + d) * load(k, enc, kvrow + d);
+            dpo += load(dout, enc, qrow + d) * load(v, enc, kvrow + d);
+        }
+        s[j] = scale * dot;
+        dp[j] = dpo;
+        if (s[j] > m) m = s[j];
+    }
+    double l = 0.0;
+    for (long j = 0; j < nvis; ++j) l += exp(s[j] - m);
+    double lse = m + log(l);
+    double delta = 0.0;
+    for (long j = 0; j < nvis; ++j) delta += exp(s[j] - lse) * dp[j];
+    if (dq_row) {
+        for (long j = 0; j < nvis; ++j) {
+            double ds = exp(s[j] - lse) * (dp[j] - delta);
+            size_t kvrow = kv_base + (size_t)j * (size_t)D;
+            for (long d = 0; d < D; ++d) dq_row[d] += scale * ds * load(k, enc, kvrow + d);
+        }
+    }
+    *lse_out = lse;
+    *delta_out = delta;
+}
+
+/* Key j of a head, given LSE_i and Delta_i of every row: over the rows that
+ * see key j, dV_j = sum_i P_ij dO_i and dK_j = scale * sum_i dS_ij q_i with
+ * dS_ij = P_ij (dP_ij - Delta_i) (same sections). */
+static void bwd_col(const void* q, const void* k, const void* v, const void* dout, int enc,
+                    long N, long D, double scale, int causal, size_t q_base, size_t kv_base,
+                    long j, const double* lse, const double* delta, double* dk_row, double* dv_row)
+{
+    size_t kvrow = kv_base + (size_t)j * (size_t)D;
+    for (long d = 0; d < D; ++d) dk_row[d] = dv_row[d] = 0.0;
+    for (long i = causal ? j : 0; i < N; ++i) {
+        if (lse[i] == -INFINITY) continue;
+        size_t qrow = q_base + (size_t)i * (size_t)D;
+        double dot = 0.0, dpo = 0.0;
+        for (long d = 0; d < D; ++d) {
+            dot += load(q, enc, qrow + d) * load(k, enc, kvrow + d);
+            dpo += load(dout, enc, qrow + d) * load(v, enc, kvrow + d);
+        }
+        double p = exp(scale * dot - lse[i]);
+        double ds = p * (dpo - delta[i]);
+        for (long d = 0; d < D; ++d) {
+            dv_row[d] += p * load(dout, enc, qrow + d);
+            dk_row[d] += scale * ds * load(q, enc, qrow + d);
+        }
+    }
+}
+
+/* LSE and Delta of every row of head bh (OpenMP over rows). */
+static int bwd_head_stats(const void* q, const void* k, const void* v, const void* dout, int enc,
+                          long N, long D, double scale, int causal, size_t base, double* lse, double* delta)
+{
+    int err = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)N);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!s || !dp) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 16)
+            for (long i = 0; i < N; ++i)
+                bwd_row(q, k, v, dout, enc, N, D, scale, causal, base, base, i, s, dp, &lse[i], &delta[i], NULL);
+        }
+        free(s);
+        free(dp);
+    }
+    return err;
+}
+
+int fa_ref_backward(const void* q, const void* k, const void* v, const void* dout, int enc,
+                    double* dq, double* dk, double* dv, double* delta_out,
+                    long B, long H, long N, long D, double scale, int causal, int nthreads)
+{
+    if (bad_args(q, k, v, enc, B, H, N, D) || !dout || !dq || !dk || !dv) return -1;
+    set_threads(nthreads);
+    double* lse = (double*)malloc(sizeof(double) * (size_t)N);
+    double* dlt = (double*)malloc(sizeof(double) * (size_t)N);
+    if (!lse || !dlt) {
+        free(lse);
+        free(dlt);
+        return -2;
+    }
+    int err = 0;
+    for (long bh = 0; bh < B * H && !err; ++bh) {
+        size_t base = (size_t)bh * (size_t)N * (size_t)D;
+#pragma omp parallel
+        {
+            double* s = (double*)malloc(sizeof(double) * (size_t)N);
+            double* dp = (double*)malloc(sizeof(double) * (size_t)N);
+            if (!s || !dp) {
+#pragma omp atomic write
+                err = 1;
+            } else {
+#pragma omp for schedule(dynamic, 16)
+                for (long i = 0; i < N; ++i)
+                    bwd_row(q, k, v, dout, enc, N, D, scale, causal, base, base, i, s, dp, &lse[i], &dlt[i],
+                            dq + base + (size_t)i * (size_t)D);
+            }
+            free(s);
+            free(dp);
+        }
+        if (err) break;
+#pragma omp parallel for schedule(dynamic, 16)
+        for (long j = 0; j < N; ++j)
+            bwd_col(q, k, v, dout, enc, N, D, scale, causal, base, base, j, lse, dlt,
+                    dk + base + (size_t)j * (size_t)D, dv + base + (size_t)j * (size_t)D);
+        if (delta_out)
+            for (long i = 0; i < N; ++i) delta_out[(size_t)bh * (size_t)N + (size_t)i] = dlt[i];
+    }
+    free(lse);
+    free(dlt);
+    return err ? -2 : 0;
+}
+
+int fa_ref_backward_sample(const void* q, const void* k, const void* v, const void* dout, int enc,
+                           long B, long H, long N, long D, double scale, int causal,
+                           const long* dq_bh, const long* dq_rows, long n_dq, double* dq_out,
+                           const long* kv_bh, const long* kv_keys, long n_kv, double* dk_out, double* dv_out,
+                           int nthreads)
+{
+    if (bad_args(q, k, v, enc, B, H, N, D) || !dout) return -1;
+    if ((n_dq > 0 && (!dq_bh || !dq_rows || !dq_out)) || (n_kv > 0 && (!kv_bh || !kv_keys || !dk_out || !dv_out)))
+        return -1;
+    for (long r = 0; r < n_dq; ++r)
+        if (dq_bh[r] < 0 || dq_bh[r] >= B * H || dq_rows[r] < 0 || dq_rows[r] >= N) return -1;
+    for (long r = 0; r < n_kv; ++r)
+        if (kv_bh[r] < 0 || kv_bh[r] >= B * H || kv_keys[r] < 0 || kv_keys[r] >= N) return -1;
+    set_threads(nthreads);
+    int err = 0;
+    /* dQ rows: each is local to its row */
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)N);
+        double* dp = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!s || !dp) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (long r = 0; r < n_dq; ++r) {
+                size_t base = (size_t)dq_bh[r] * (size_t)N * (size_t)D;
+                double lse_r, dlt_r;
+                bwd_row(q, k, v, dout, enc, N, D, scale, causal, base, base, dq_rows[r], s, dp, &lse_r, &dlt_r,
+                        dq_out + (size_t)r * (size_t)D);
+            }
+        }
+        free(s);
+        free(dp);
+    }
+    if (err) return -2;
+    /* dK / dV keys: the row statistics of each sampled head, then the columns */
+    if (n_kv > 0) {
+        double* lse = (double*)malloc(sizeof(double) * (size_t)N);
+        double* dlt = (double*)malloc(sizeof(double) * (size_t)N);
+        if (!lse || !dlt) {
+            free(lse);
+            free(dlt);
+            return -2;
+        }
+        for (long bh = 0; bh < B * H && !err; ++bh) {
+            int used = 0;
+            for (long r = 0; r < n_kv && !used; ++r) used = kv_bh[r] == bh;
+            if (!used) continue;
+            size_t base = (size_t)bh * (size_t)N * (size_t)D;
+            err = bwd_head_stats(q, k, v, dout, enc, N, D, scale, causal, base, lse, dlt);
+            if (err) break;
+#pragma omp parallel for schedule(dynamic, 1)
+            for (long r = 0; r < n_kv; ++r)
+                if (kv_bh[r] == bh)
+                    bwd_col(q, k, v, dout, enc, N, D, scale, causal, base, base, kv_keys[r], lse, dlt,
+                            dk_out + (size_t)r * (size_t)D, dv_out + (size_t)r * (size_t)D);
+        }
+        free(lse);
+        free(dlt);
+    }
+    return err ? -2 : 0;
 }

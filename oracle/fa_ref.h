@@ -1,5 +1,6 @@
 /*
- * fa_ref.h -- FP64 CPU oracle for the exact attention forward pass.
+ * fa_ref.h -- FP64 CPU oracle for the exact attention forward and backward
+ * passes.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
  * baseline leg of the bench may load this library.  It shares no code, header
@@ -103,6 +104,33 @@ int fa_ref_naive_gqa(const void* q, const void* k, const void* v, int enc,
                      double* o, double* lse,
                      long B, long H, long H_kv, long N, long D, double scale, int causal,
                      int nthreads);
+
+/* Backward pass ("Why FlashAttention does not need to store the attention
+ * matrix", section 3.3; "CUDA FlashAttention: from online softmax to the
+ * long-sequence IO limit", section 4.3.1).  With G = dO = dL/dO (the same
+ * encoding as q, k, v) and P = softmax(scale * Q K^T + M) row by row:
+ *     dV    = P^T dO
+ *     dP    = dO V^T
+ *     Delta = rowsum(dP (x) P)                      (one value per query row)
+ *     dS    = P (x) (dP - Delta)
+ *     dQ    = scale * dS K,    dK = scale * dS^T Q
+ * P_ij is rebuilt as exp(s_ij - LSE_i) from the row's log-sum-exp.  No N x N
+ * matrix is stored: one pass over the query rows gives LSE, Delta and dQ, a
+ * second pass over the keys gives dK and dV.  dq, dk, dv are [B,H,N,D];
+ * delta_out ([B,H,N]) may be NULL. */
+int fa_ref_backward(const void* q, const void* k, const void* v, const void* dout, int enc,
+                    double* dq, double* dk, double* dv, double* delta_out,
+                    long B, long H, long N, long D, double scale, int causal, int nthreads);
+
+/* The same gradients on selected entries only: dQ of query row dq_rows[r] of
+ * head dq_bh[r] -> dq_out[r*D ...]; dK and dV of key kv_keys[r] of head
+ * kv_bh[r] -> dk_out / dv_out [r*D ...].  Costs O(N*D) per dQ row, plus one
+ * O(N^2*D) pass of row statistics per head that has sampled keys. */
+int fa_ref_backward_sample(const void* q, const void* k, const void* v, const void* dout, int enc,
+                           long B, long H, long N, long D, double scale, int causal,
+                           const long* dq_bh, const long* dq_rows, long n_dq, double* dq_out,
+                           const long* kv_bh, const long* kv_keys, long n_kv, double* dk_out, double* dv_out,
+                           int nthreads);
 
 /* Threads the OpenMP runtime would use for nthreads <= 0. */
 int fa_ref_max_threads(void);

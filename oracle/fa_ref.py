@@ -59,6 +59,11 @@ def _load():
         lib.fa_ref_split_merge.restype = I
         lib.fa_ref_naive_gqa.argtypes = [vp, vp, vp, I, dp, dp, L, L, L, L, L, Dbl, I, I]
         lib.fa_ref_naive_gqa.restype = I
+        lib.fa_ref_backward.argtypes = [vp, vp, vp, vp, I, dp, dp, dp, dp, L, L, L, L, Dbl, I, I]
+        lib.fa_ref_backward.restype = I
+        lib.fa_ref_backward_sample.argtypes = [vp, vp, vp, vp, I, L, L, L, L, Dbl, I, lp, lp, L, dp,
+                                               lp, lp, L, dp, dp, I]
+        lib.fa_ref_backward_sample.restype = I
         lib.fa_ref_max_threads.argtypes = []
         lib.fa_ref_max_threads.restype = I
         _lib = lib
@@ -196,3 +201,59 @@ def naive_gqa(q, k, v, scale, causal=False, enc="f64", nthreads=0):
     if rc != 0:
         raise RuntimeError("fa_ref_naive_gqa failed (%d)" % rc)
     return o, lse
+
+
+def backward(q, k, v, dout, scale, causal=False, enc="f64", nthreads=0):
+    """Gradients of attention for the upstream gradient dout = dL/dO.
+
+    Returns (dQ, dK, dV, Delta): dQ, dK, dV [B,H,N,D] and Delta [B,H,N]
+    (Delta_i = rowsum(dP_i * P_i)), all float64."""
+    q, k, v = _prep(q, k, v, enc)
+    (g,) = _prep_like(dout, q, enc)
+    B, H, N, D = q.shape
+    dq = np.empty((B, H, N, D), np.float64)
+    dk = np.empty((B, H, N, D), np.float64)
+    dv = np.empty((B, H, N, D), np.float64)
+    delta = np.empty((B, H, N), np.float64)
+    rc = _load().fa_ref_backward(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data, ENC[enc],
+                                 _dptr(dq), _dptr(dk), _dptr(dv), _dptr(delta), B, H, N, D, float(scale),
+                                 int(bool(causal)), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("fa_ref_backward failed (%d)" % rc)
+    return dq, dk, dv, delta
+
+
+def backward_sample(q, k, v, dout, scale, causal, dq_bh, dq_rows, kv_bh, kv_keys, enc="f64", nthreads=0):
+    """Selected gradient rows: returns (dQ [R,D] of (dq_bh[r], dq_rows[r]),
+    dK [S,D] and dV [S,D] of (kv_bh[s], kv_keys[s]))."""
+    q, k, v = _prep(q, k, v, enc)
+    (g,) = _prep_like(dout, q, enc)
+    B, H, N, D = q.shape
+    lp = ctypes.POINTER(ctypes.c_long)
+    a_bh, a_rows, b_bh, b_keys = (np.ascontiguousarray(x, dtype=np.int64) for x in (dq_bh, dq_rows, kv_bh, kv_keys))
+    if a_bh.shape != a_rows.shape or b_bh.shape != b_keys.shape:
+        raise ValueError("index arrays of a pair must have the same length")
+    R, S = a_bh.shape[0], b_bh.shape[0]
+    dq = np.empty((max(R, 1), D), np.float64)
+    dk = np.empty((max(S, 1), D), np.float64)
+    dv = np.empty((max(S, 1), D), np.float64)
+    rc = _load().fa_ref_backward_sample(q.ctypes.data, k.ctypes.data, v.ctypes.data, g.ctypes.data, ENC[enc],
+                                        B, H, N, D, float(scale), int(bool(causal)),
+                                        a_bh.ctypes.data_as(lp), a_rows.ctypes.data_as(lp), R, _dptr(dq),
+                                        b_bh.ctypes.data_as(lp), b_keys.ctypes.data_as(lp), S, _dptr(dk), _dptr(dv),
+                                        int(nthreads))
+    if rc != 0:
+        raise RuntimeError("fa_ref_backward_sample failed (%d)" % rc)
+    return dq[:R], dk[:S], dv[:S]
+
+
+def _prep_like(t, ref, enc):
+    want = np.float64 if enc == "f64" else np.uint16
+    a = np.ascontiguousarray(t)
+    if a.dtype != want:
+        raise TypeError("enc=%s needs %s arrays, got %s" % (enc, np.dtype(want), a.dtype))
+    if a.ndim == 2:
+        a = a.reshape(1, 1, *a.shape)
+    if a.shape != ref.shape:
+        raise ValueError("dout must have the shape of q")
+    return (a,)
