@@ -1,10 +1,11 @@
-"""Exact attention forward pass on GB300 (sm_103a).
+"""Exact attention forward and backward passes on GB300 (sm_103a).
 
 The compute path is the CUDA library ``libfa.so`` (built from ``csrc/``); this
 package only marshals arguments to its C ABI (``include/fa.h``).  There is no
 CPU or PyTorch fallback: if the library is missing, importing the binding
 raises.
 """
-from .binding import (FA_BF16, FA_FP16, FA_OK, FaError, STATUS_NAMES, attention, fa_fwd,  # noqa: F401
-                      fa_fwd_gqa, fa_fwd_splitkv, fa_fwd_splitkv_noalloc, fa_get_device_status, fa_noalloc_scratch_bytes, fa_selftest_wait_timeout,
+from .binding import (FA_BF16, FA_FP16, FA_OK, FaError, STATUS_NAMES, attention, attention_backward,  # noqa: F401
+                      fa_bwd, fa_bwd_workspace_bytes, fa_fwd, fa_fwd_gqa, fa_fwd_splitkv, fa_fwd_splitkv_noalloc,
+                      fa_get_device_status, fa_noalloc_scratch_bytes, fa_selftest_wait_timeout,
                       fa_splitkv_workspace_bytes, fa_status_string, library_path, load_library)

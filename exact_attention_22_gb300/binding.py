@@ -58,6 +58,10 @@ def load_library():
         lib.fa_noalloc_scratch_bytes.restype = ctypes.c_size_t
         lib.fa_selftest_wait_timeout.argtypes = [vp]
         lib.fa_selftest_wait_timeout.restype = I
+        lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
+        lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, I, vp, ctypes.c_size_t, vp]
+        lib.fa_bwd.restype = I
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -100,6 +104,17 @@ def fa_fwd_splitkv_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H: 
 
 def fa_noalloc_scratch_bytes() -> int:
     return int(load_library().fa_noalloc_scratch_bytes())
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    return int(load_library().fa_bwd_workspace_bytes(B, H, N, D))
+
+
+def fa_bwd(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int, B: int, H: int, N: int,
+           D: int, scale: float, causal: int, dtype: int, workspace: int, workspace_bytes: int, stream: int) -> int:
+    """Direct call of the backward entry point; returns its status code."""
+    return int(load_library().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, D, float(scale), int(causal),
+                                     int(dtype), workspace, int(workspace_bytes), stream))
 
 
 def fa_get_device_status(stream: int) -> int:
@@ -173,3 +188,43 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
     return out, lse
+
+
+def attention_backward(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None,
+                       dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of attention for contiguous fp16/bf16 CUDA tensors [B,H,N,D]:
+    ``out`` and ``lse`` are the forward pass's outputs, ``dout`` the upstream
+    gradient.  Gradients (and the workspace) are allocated with torch when not
+    given.  Raises FaError on a non-OK status.  Asynchronous on ``stream``."""
+    import torch
+
+    ts = (q, k, v, out, dout)
+    if not all(t.is_cuda for t in ts) or not lse.is_cuda:
+        raise ValueError("all tensors must be CUDA tensors")
+    if q.dtype not in (torch.float16, torch.bfloat16) or any(t.dtype != q.dtype for t in ts):
+        raise ValueError("q, k, v, out, dout must share one dtype, float16 or bfloat16")
+    if q.dim() != 4 or any(t.shape != q.shape for t in ts):
+        raise ValueError("q, k, v, out, dout must all be [B, H, N, D]")
+    B, H, N, D = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be float32 [B, H, N]")
+    if not all(t.is_contiguous() for t in ts + (lse,)):
+        raise ValueError("inputs must be contiguous")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = fa_bwd_workspace_bytes(B, H, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    dt = FA_BF16 if q.dtype == torch.bfloat16 else FA_FP16
+    st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D, scale, int(bool(causal)), dt,
+                workspace.data_ptr(), workspace.numel() * workspace.element_size(), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv

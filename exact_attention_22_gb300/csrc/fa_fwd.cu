@@ -47,6 +47,7 @@
 
 #include "fa.h"
 #include "sm103_ptx.cuh"
+#include "fa_host.cuh"
 
 namespace fa103 {
 
@@ -833,49 +834,6 @@ __global__ void __launch_bounds__(32) selftest_wait_timeout_kernel() {
 
 // ------------------------------------------------------------------ host
 
-static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-static std::once_flag g_encode_once;
-
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    std::call_once(g_encode_once, [] {
-        void* fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    return g_encode;
-}
-
-// [B*H, N, D] view, 128-row x 64-column boxes with the 128-byte swizzle.
-static bool make_tile_map(CUtensorMap* map, const void* base, int dtype, int D, int N, int BH) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(N) * D * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTileM), 1};
-    cuuint32_t elem_strides[3] = {1, 1, 1};
-    CUresult r = enc(map, dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                     const_cast<void*>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
-// Streaming multiprocessors of a device (cached per device).
-static int sm_count(int dev) {
-    static std::atomic<int> cache[64];
-    if (dev >= 0 && dev < 64) {
-        const int c = cache[dev].load();
-        if (c > 0) return c;
-    }
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return -1;
-    if (dev >= 0 && dev < 64) cache[dev].store(n);
-    return n;
-}
-
 template <int D, bool BF16, bool CAUSAL, bool SPLIT>
 static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
                           cudaStream_t stream) {
@@ -895,11 +853,6 @@ static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUte
     const unsigned grid = static_cast<unsigned>(p.n_tiles < sms ? p.n_tiles : sms);
     kern<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(q, k, v, p);
     return cudaGetLastError();
-}
-
-static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
-    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + nb && y < x + na;
 }
 
 }  // namespace fa103
@@ -1101,14 +1054,15 @@ extern "C" int fa_selftest_wait_timeout(cudaStream_t stream) {
 
 extern "C" int fa_get_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
-    unsigned int v = 0;
+    unsigned int v = 0, vb = 0;
     if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof v) != cudaSuccess) return FA_ERR_CUDA;
+    if (bwd_take_status(&vb) != 0) return FA_ERR_CUDA;
     if (v != 0) {
         const unsigned int zero = 0;
         if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof zero) != cudaSuccess) return FA_ERR_CUDA;
-        return FA_ERR_TIMEOUT;
     }
-    return FA_OK;
+    if (vb & kBwdStatusLayout) return FA_ERR_CUDA;
+    return (v | vb) != 0 ? FA_ERR_TIMEOUT : FA_OK;
 }
 
 extern "C" const char* fa_status_string(int status) {

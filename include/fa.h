@@ -151,11 +151,55 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
 size_t fa_noalloc_scratch_bytes(void);
 
 /*
+ * fa_bwd_workspace_bytes -- bytes of workspace fa_bwd needs for these sizes:
+ * an fp32 dQ accumulator (4*B*H*N*D bytes) and one fp32 value per query row
+ * (4*B*H*N), each rounded up to 256 bytes.  Returns 0 for invalid sizes (any
+ * size < 1, D not 64 or 128).
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int D);
+
+/*
+ * fa_bwd -- the backward pass ("Why FlashAttention does not need to store the
+ * attention matrix", section 3.3; "CUDA FlashAttention: from online softmax to
+ * the long-sequence IO limit", sections 4.3.1-4.3.2): given the upstream
+ * gradient dO = dL/dO of the forward pass O = softmax(scale*Q K^T + M) V, it
+ * rebuilds P from the forward's LSE tile by tile (no N x N matrix is stored)
+ * and computes
+ *     dV = P^T dO,   dP = dO V^T,   dS = P (x) (dP - Delta),
+ *     dQ = scale * dS K,   dK = scale * dS^T Q,
+ * with Delta_i = rowsum(dP_i (x) P_i), evaluated as dO_i . O_i from the
+ * forward's output O (the two are equal because every row of P sums to 1).
+ *
+ *   q, k, v     [B,H,N,D] inputs of the forward pass, type `dtype` (device, read)
+ *   o           [B,H,N,D] the forward's output O                  (device, read)
+ *   dout        [B,H,N,D] dO, type `dtype`                        (device, read)
+ *   lse         [B,H,N] fp32, the forward's natural-log LSE       (device, read)
+ *   dq, dk, dv  [B,H,N,D] gradients, type `dtype`                 (device, written)
+ *   workspace   DEVICE memory owned by the caller, 16-byte aligned, at least
+ *               fa_bwd_workspace_bytes(B, H, N, D) bytes; overwritten (dQ is
+ *               accumulated there in fp32 before it is rounded into dq)
+ *   B, H, N, D, scale, causal, dtype, stream   as for fa_fwd; scale and causal
+ *               must be the values the forward pass used
+ *
+ * Returns FA_OK once the three kernels are queued on `stream`.  Argument
+ * errors are reported before anything is launched: FA_ERR_MISALIGNED for a
+ * null or misaligned pointer, FA_ERR_UNSUPPORTED for D other than 64 or 128,
+ * FA_ERR_INVALID_ARG for bad sizes, a small workspace, or outputs (dq, dk, dv,
+ * workspace) that overlap the inputs or each other.  dQ is summed with fp32
+ * atomic additions, so its last bits may differ between runs; dK and dV are
+ * deterministic.  Calls that share a workspace must not overlap in time.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+           void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale, int causal, int dtype,
+           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fa_get_device_status -- synchronise `stream`, then report whether any
  * kernel of this library on the current device gave up on a bounded wait
  * since the last call (FA_ERR_TIMEOUT; the outputs of that launch are
- * undefined), or whether the stream holds a CUDA error (FA_ERR_CUDA).
- * Reading the status clears it.
+ * undefined), or whether the stream holds a CUDA error (FA_ERR_CUDA; also
+ * reported if a backward kernel found its shared memory misaligned and did
+ * nothing).  Reading the status clears it.
  */
 int fa_get_device_status(cudaStream_t stream);
 

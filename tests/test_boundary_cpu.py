@@ -98,3 +98,45 @@ def test_splitkv_argument_errors_without_gpu(lib, splits, ws, ws_bytes, status):
 def test_gqa_head_count_errors(lib, H, H_kv, status):
     a = GOOD
     assert fa.fa_fwd_gqa(a["q"], a["k"], a["v"], a["o"], a["lse"], 1, H, H_kv, 256, 64, 0.125, 0, 0, 0) == status
+
+
+def test_bwd_workspace_size(lib):
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_bytes(2, 3, 100, 128) == r256(600 * 128 * 4) + r256(600 * 4)
+    assert fa.fa_bwd_workspace_bytes(1, 1, 1, 64) == 256 + 256
+    for bad in ((0, 1, 1, 64), (1, 0, 1, 64), (1, 1, 0, 64), (1, 1, 1, 96)):
+        assert fa.fa_bwd_workspace_bytes(*bad) == 0
+
+
+# Fake aligned addresses 1 MiB apart (each tensor of B1 H2 N256 D64 is 64 KiB).
+BWD = dict(q=1 << 20, k=2 << 20, v=3 << 20, o=4 << 20, dout=5 << 20, lse=6 << 20, dq=7 << 20, dk=8 << 20,
+           dv=9 << 20, ws=10 << 20, ws_bytes=1 << 20, B=1, H=2, N=256, D=64, scale=0.125, causal=1, dtype=0)
+
+
+def _bwd(**kw):
+    a = dict(BWD, **kw)
+    return fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"], a["B"], a["H"],
+                     a["N"], a["D"], a["scale"], a["causal"], a["dtype"], a["ws"], a["ws_bytes"], 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), 2), (dict(D=256), 2),
+    (dict(B=0), 1), (dict(N=-3), 1), (dict(causal=2), 1), (dict(dtype=5), 1),
+    (dict(scale=0.0), 1), (dict(scale=math.nan), 1),
+    (dict(dq=0), 3), (dict(lse=0), 3), (dict(ws=0), 3), (dict(dout=(5 << 20) + 8), 3), (dict(ws=(10 << 20) + 4), 3),
+    (dict(ws_bytes=1024), 1),                  # workspace too small
+    (dict(dq=(1 << 20) + 1024), 1),            # dq overlaps q
+    (dict(dk=(9 << 20) - 4096), 1),            # dk overlaps dv
+    (dict(ws=(6 << 20) - 256), 1),             # workspace overlaps lse
+    (dict(dv=(4 << 20) + 16), 1),              # dv overlaps o
+])
+def test_bwd_argument_errors_without_gpu(lib, kw, status):
+    assert _bwd(**kw) == status
+
+
+def test_bwd_binding_rejects_bad_tensors(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    lse = torch.zeros(1, 1, 8)
+    with pytest.raises(ValueError):
+        fa.attention_backward(x, x, x, x, lse, x)
