@@ -6,6 +6,7 @@ O += PV, the O / l and LSE epilogue).  Default workload: B=1, H=32, N=8192,
 D=128, causal, fp16 -- the configuration the throughput target is quoted on.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+    python bench.py --pass bwd ...      the backward pass (fa_bwd) on the same workloads
 
 Metric: attention forward TFLOP/s with the causal-adjusted FLOP model
 (4*B*H*N^2*D, halved when causal), whole job over all ranks.
@@ -366,6 +367,140 @@ def run_ours(args, w):
     return 0
 
 
+def run_ours_bwd(args, w):
+    """The backward pass (fa_bwd: Delta kernel, main kernel, dQ conversion) on
+    the same workload: one step = one fa_bwd call; FLOPs = 2.5x the forward's
+    (five N x N x D GEMMs -- S, dP, dV, dK, dQ -- against the forward's two)."""
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_22_gb300 as fa
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    q_h, k_h, v_h = fa_inputs.make_qkv(w, seed=args.seed + rank)
+    g = torch.Generator().manual_seed(args.seed + rank + 1000)
+    do_h = torch.randn(q_h.shape, generator=g).to(q_h.dtype)
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o, lse = fa.attention(q, k, v, causal=w.causal, scale=w.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws_bytes = fa.fa_bwd_workspace_bytes(w.B, w.H, w.N, w.D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream
+    dt = fa.FA_BF16 if w.dtype == "bf16" else fa.FA_FP16
+    flops = 2.5 * w.flops
+
+    def launch():
+        st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                       dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N, w.D, w.scale, int(w.causal), dt,
+                       ws.data_ptr(), ws_bytes, handle)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_bwd")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize()
+    status = fa.fa_get_device_status(handle)
+    if status != fa.FA_OK:
+        raise fa.FaError(status, "warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    status = fa.fa_get_device_status(handle)
+    if status != fa.FA_OK:
+        raise fa.FaError(status, "timed region")
+
+    # End to end: H2D of Q, K, V, O, dO, LSE; the call; D2H of dQ, dK, dV.
+    pins = [t.pin_memory() for t in (q_h, k_h, v_h, o.cpu(), do_h, lse.cpu())]
+    devs = [q, k, v, o, do, lse]
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+    e2e_steps = max(3, min(args.steps, 30))
+
+    def e2e_step():
+        for d_, h_ in zip(devs, pins):
+            d_.copy_(h_, non_blocking=True)
+        launch()
+        for h_, d_ in zip(outs_h, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in devs)
+    d2h = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
+
+    total_ms, e2e_ms = max_over_ranks([sum(step_ms), e2e_ms], device=dev)
+    ms_per_step = total_ms / args.steps
+    value = job_tflops(world, flops, ms_per_step)
+    peak, hbm, peak_kind = measured_peaks()
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    line = {
+        "metric": "attention bwd TFLOP/s (causal-adjusted, 2.5x the forward FLOPs)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) inputs and dO, see fa_inputs.py)",
+        "config": {"workload": w.name, "pass": "bwd", "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+                   "scale": w.scale, "parallelism": "replica per GPU" if world > 1 else "single GPU",
+                   "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                   "ms_p50": statistics.median(step_ms), "ms_min": min(step_ms), "entry": "fa_bwd"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": "%s dense bf16 (burst); fp16/bf16 nominal ratio 1" % peak_kind},
+        "e2e": {"value": job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+        "kernel_source_sha": kernel_source_hash(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import fa_ref
+
+        e = fa_inputs.enc(w)
+        one = [fa_inputs.bits(t[:1, :1]) for t in (q_h, k_h, v_h, do_h)]
+        t0 = time.time()
+        fa_ref.backward(*one, w.scale, w.causal, enc=e)
+        secs = time.time() - t0
+        line["cpu_baseline"] = {
+            "value": flops / (w.B * w.H) / secs / 1e12, "unit": "TFLOP/s", "cores": fa_ref.max_threads(),
+            "kind": "oracle", "sample": "head (0, 0) of the workload: every row and key, FP64 backward oracle, "
+                                        "%.1f s" % secs}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -378,12 +513,16 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="time fa_fwd_splitkv with this many K/V chunks per query block (0: fa_fwd)")
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
+                    help="time the forward pass (default, the headline) or the backward pass")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = fa_inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.which == "bwd":
+        return run_ours_bwd(args, w)
     return run_ours(args, w)
 
 
