@@ -23,14 +23,14 @@
 //   * dQ^T = K^T dS^T (TMEM lane = head-dim index) reads dS^T from shared
 //     memory, where the compute warps also write it in the 128-byte-swizzled
 //     layout the tensor core reads.  A dQ warpgroup loads dQ^T from TMEM and
-//     adds scale * dQ^T into the fp32 accumulator with red.global.add;
+//     adds scale * dQ^T into the fp32 accumulator with red.global.add, whole
+//     128-byte lines per warp instruction;
 //   * K_j and V_j are loaded once per work tile; Q_i and dO_i stream through
 //     two-slot rings; LSE_i (in log2 units) and Delta_i through a two-stage
 //     buffer filled by a loader warp;
 //   * one warp issues every UMMA (elect.sync), two compute warpgroups each own
 //     64 query columns of every key row, and the fourth warpgroup drains dQ.
-// For D = 64 the dQ^T UMMA runs with M = 128: TMEM lanes 64..127 then hold
-// products of the next tile in shared memory and are never read.
+// For D = 64, dQ is computed untransposed (dQ = dS K) and added row by row.
 // Every mbarrier wait is bounded in time, as in the forward kernel.
 
 #include <cuda.h>
@@ -289,7 +289,10 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
     const int lane = threadIdx.x & 31;
     constexpr uint32_t kIdS = idesc_f16_ab(BF16, kTile, kTile, false, false);   // S^T, dP^T
     constexpr uint32_t kIdG = idesc_f16_ab(BF16, kTile, D, false, true);        // dV, dK (A in TMEM)
-    constexpr uint32_t kIdQ = idesc_f16_ab(BF16, kTile, kTile, true, true);     // dQ^T
+    // dQ: for D = 128 as dQ^T = K^T dS^T (M = head dim, N = queries), for D = 64
+    // as dQ = dS K (M = queries, N = 64): see run_dq.
+    constexpr uint32_t kIdQ = D == 128 ? idesc_f16_ab(BF16, kTile, kTile, true, true)
+                                       : idesc_f16_ab(BF16, kTile, D, true, true);
     constexpr int kSteps = D / 16;   // K-steps over the head dimension
     const uint64_t dK = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
     const uint64_t dV = sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
@@ -360,10 +363,15 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
                 umma_ts_elect(tmem + C::kTmDK, tmem + C::kTmB + acol(kk), dQmn[slot] + 128 * kk, kIdG,
                               (s > 0 || kk > 0) ? 1u : 0u);
             umma_commit_elect(&st.q_empty[slot]);
-            // dQ^T: K-step kk over the keys reads 16 rows of K (A, MN-major) and of dS^T (B, MN-major)
+            // dQ^T = K^T dS^T (D = 128) or dQ = dS K (D = 64): K-step kk over the keys reads 16
+            // rows of K and of dS^T, both stored with the M or N index contiguous (MN-major)
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-                umma_ss_elect(tmem + C::kTmA, dKmn + 128 * kk, dDSmn + 128 * kk, kIdQ, kk > 0);
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+                if constexpr (D == 128)
+                    umma_ss_elect(tmem + C::kTmA, dKmn + 128 * kk, dDSmn + 128 * kk, kIdQ, kk > 0);
+                else
+                    umma_ss_elect(tmem + C::kTmA, dDSmn + 128 * kk, dKmn + 128 * kk, kIdQ, kk > 0);
+            }
             umma_commit_elect(&st.dq_full);
         }
         if (!ok) break;
@@ -499,16 +507,29 @@ __device__ void run_compute(State& st, uint8_t* smem, uint32_t tmem, int wg, con
     if (!ok && lane == 0) give_up(st, ST_COMPUTE);
 }
 
-// dQ warpgroup: TMEM lane = head-dim index d.  Per step it loads dQ^T (128
-// query columns), frees TMEM, then adds scale * dQ into the fp32 accumulator.
-// Each warp instruction covers 32 consecutive d of one query row: 128 bytes.
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// dQ warpgroup.  Per step it loads the step's dQ from TMEM, frees TMEM, then
+// adds scale * dQ into the fp32 accumulator with red.global.add.  The L2
+// reduction rate, not the instruction count, bounds this: measured on GB300,
+// reductions that cover whole 128-byte lines per warp instruction beat 16-byte
+// vector reductions scattered over 32 rows.  So:
+//   D = 128: TMEM holds dQ^T (lane = head-dim index d, column = query); one
+//            warp instruction adds 32 consecutive d of one query row;
+//   D = 64:  TMEM holds dQ (lane = query row, 64 columns); each thread adds its
+//            row with 16-byte vector reductions (the transposed form would
+//            need M = 128 for 64 head-dim rows and leave half the lanes idle).
 template <int D, bool CAUSAL>
 __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
     using C = Cfg<D>;
     volatile int* abort_flag = &st.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
-    const int d = 32 * quarter + lane;
+    const int r = 32 * quarter + lane;   // TMEM lane: d (D = 128) or query row (D = 64)
     const uint32_t tA = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + C::kTmA;
+    constexpr int kCols = D == 128 ? kTile : D;   // TMEM columns of the step's dQ
     int g = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -519,29 +540,36 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
             ok = wait_warp(&st.dq_full, g & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            uint32_t v0[32], v1[32], v2[32], v3[32];
-            tmem_ld32_nowait(tA + 0, v0);
-            tmem_ld32_nowait(tA + 32, v1);
-            tmem_ld32_nowait(tA + 64, v2);
-            tmem_ld32_nowait(tA + 96, v3);
-            tmem_ld_wait_regs(v0);
-            regs_after_wait(v1);
-            regs_after_wait(v2);
-            regs_after_wait(v3);
+            uint32_t v[kCols / 32][32];
+#pragma unroll
+            for (int c = 0; c < kCols / 32; ++c) tmem_ld32_nowait(tA + 32 * c, v[c]);
+            tmem_ld_wait_regs(v[0]);
+#pragma unroll
+            for (int c = 1; c < kCols / 32; ++c) regs_after_wait(v[c]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&st.dq_free);
-            if (d < D) {
-                const int q0 = (w.i0 + s) * kTile;
+            const int q0 = (w.i0 + s) * kTile;
+            const float sc = p.scale;
+            if constexpr (D == 128) {
                 const int nq = p.N - q0 < kTile ? p.N - q0 : kTile;
-                float* base = p.dq_acc + (static_cast<size_t>(w.bh) * p.N + q0) * D + d;
-                const float sc = p.scale;
+                float* base = p.dq_acc + (static_cast<size_t>(w.bh) * p.N + q0) * D + r;
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    if (c < nq) atomicAdd(base + static_cast<size_t>(c) * D, __uint_as_float(v0[c]) * sc);
-                    if (c + 32 < nq) atomicAdd(base + static_cast<size_t>(c + 32) * D, __uint_as_float(v1[c]) * sc);
-                    if (c + 64 < nq) atomicAdd(base + static_cast<size_t>(c + 64) * D, __uint_as_float(v2[c]) * sc);
-                    if (c + 96 < nq) atomicAdd(base + static_cast<size_t>(c + 96) * D, __uint_as_float(v3[c]) * sc);
+#pragma unroll
+                    for (int part = 0; part < 4; ++part)
+                        if (c + 32 * part < nq)
+                            atomicAdd(base + static_cast<size_t>(c + 32 * part) * D, __uint_as_float(v[part][c]) * sc);
+                }
+            } else {
+                if (q0 + r < p.N) {
+                    float* row = p.dq_acc + (static_cast<size_t>(w.bh) * p.N + q0 + r) * D;
+#pragma unroll
+                    for (int c = 0; c < kCols / 32; ++c)
+#pragma unroll
+                        for (int e = 0; e < 32; e += 4)
+                            red_add_v4(row + 32 * c + e, __uint_as_float(v[c][e]) * sc, __uint_as_float(v[c][e + 1]) * sc,
+                                       __uint_as_float(v[c][e + 2]) * sc, __uint_as_float(v[c][e + 3]) * sc);
                 }
             }
         }
