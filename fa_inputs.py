@@ -95,3 +95,35 @@ def enc(w_or_dtype) -> str:
     """Oracle encoding name for a workload or a torch dtype."""
     d = w_or_dtype.torch_dtype if isinstance(w_or_dtype, Workload) else w_or_dtype
     return "f16" if d == torch.float16 else "bf16"
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3_blocks(x, block_rows=128):
+    """Per-block FP8 quantization of x [B,H,N,D] (float): for every block of
+    block_rows rows of a head, scale = amax / 448 (1 for an all-zero block) and
+    q = E4M3(x / scale), rounded to nearest even by torch's float8_e4m3fn cast.
+    Returns (q as uint8 bit patterns [B,H,N,D], scales float32 [B,H,nb])."""
+    B, H, N, D = x.shape
+    nb = (N + block_rows - 1) // block_rows
+    xf = x.float()
+    pad = nb * block_rows - N
+    xp = torch.nn.functional.pad(xf, (0, 0, 0, pad)) if pad else xf
+    amax = xp.reshape(B, H, nb, block_rows * D).abs().amax(dim=-1)
+    scales = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).float()
+    rows_scale = scales.repeat_interleave(block_rows, dim=2)[:, :, :N, None]
+    q8 = (xf / rows_scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return q8.view(torch.uint8), scales
+
+
+def make_qkv_fp8(w, seed=0):
+    """N(0,1) Q, K, V of workload w (drawn as in make_qkv, before any cast),
+    quantized per 128-row block: ((q8, k8, v8) uint8 [B,H,N,D], (qs, ks, vs))."""
+    g = torch.Generator().manual_seed(seed)
+    shape = (w.B, w.H, w.N, w.D)
+    q = torch.randn(shape, generator=g) * w.qk_std
+    k = torch.randn(shape, generator=g) * w.qk_std
+    v = torch.randn(shape, generator=g)
+    out = [quantize_e4m3_blocks(t) for t in (q, k, v)]
+    return tuple(o[0] for o in out), tuple(o[1] for o in out)

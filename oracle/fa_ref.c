@@ -653,3 +653,36 @@ int fa_ref_backward_sample(const void* q, const void* k, const void* v, const vo
     }
     return err ? -2 : 0;
 }
+
+/* ---- FP8 (E4M3) inputs with per-block scales ---------------------------- */
+
+/* OCP 8-bit E4M3 ("FN": no infinities): 1 sign bit, 4 exponent bits (bias 7),
+ * 3 fraction bits; exponent 0 is subnormal (f * 2^-9); S.1111.111 is NaN. */
+double fa_ref_decode_e4m3(uint8_t x)
+{
+    int sign = (x >> 7) & 1;
+    int e = (x >> 3) & 0xf;
+    int f = x & 7;
+    double mag;
+    if (e == 15 && f == 7)
+        mag = NAN;
+    else if (e == 0)
+        mag = ldexp((double)f, -9);
+    else
+        mag = ldexp((double)(8 + f), e - 10);     /* (1.f) * 2^(e-7) */
+    return sign ? -mag : mag;
+}
+
+int fa_ref_dequant_e4m3(const uint8_t* x, const float* block_scale, long BH, long N, long D, long block_rows,
+                        double* out)
+{
+    if (!x || !block_scale || !out || BH < 1 || N < 1 || D < 1 || block_rows < 1) return -1;
+    long nb = (N + block_rows - 1) / block_rows;
+    for (long bh = 0; bh < BH; ++bh)
+        for (long n = 0; n < N; ++n) {
+            double s = (double)block_scale[bh * nb + n / block_rows];
+            size_t row = ((size_t)bh * (size_t)N + (size_t)n) * (size_t)D;
+            for (long d = 0; d < D; ++d) out[row + d] = fa_ref_decode_e4m3(x[row + d]) * s;
+        }
+    return 0;
+}

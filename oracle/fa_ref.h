@@ -26,6 +26,8 @@
 #ifndef FA_REF_H
 #define FA_REF_H
 
+#include <stdint.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -131,6 +133,18 @@ int fa_ref_backward_sample(const void* q, const void* k, const void* v, const vo
                            const long* dq_bh, const long* dq_rows, long n_dq, double* dq_out,
                            const long* kv_bh, const long* kv_keys, long n_kv, double* dk_out, double* dv_out,
                            int nthreads);
+
+/* FP8 inputs ("CUDA FlashAttention: from online softmax to the long-sequence
+ * IO limit", section 2: 8-bit Q/K/V need a per-tensor or per-block scale; the
+ * softmax state stays FP32).  fa_ref_decode_e4m3 decodes one OCP E4M3 byte
+ * exactly.  fa_ref_dequant_e4m3 turns x [BH, N, D] E4M3 with one fp32 scale
+ * per block of block_rows rows of a head (block_scale [BH, ceil(N/block_rows)])
+ * into double: out = decode(x) * scale, exact.  The attention of the
+ * dequantized values is then the plain definition above (fa_ref_naive* with
+ * FA_REF_ENC_F64). */
+double fa_ref_decode_e4m3(uint8_t x);
+int fa_ref_dequant_e4m3(const uint8_t* x, const float* block_scale, long BH, long N, long D, long block_rows,
+                        double* out);
 
 /* Threads the OpenMP runtime would use for nthreads <= 0. */
 int fa_ref_max_threads(void);

@@ -64,6 +64,10 @@ def _load():
         lib.fa_ref_backward_sample.argtypes = [vp, vp, vp, vp, I, L, L, L, L, Dbl, I, lp, lp, L, dp,
                                                lp, lp, L, dp, dp, I]
         lib.fa_ref_backward_sample.restype = I
+        lib.fa_ref_decode_e4m3.argtypes = [ctypes.c_uint8]
+        lib.fa_ref_decode_e4m3.restype = Dbl
+        lib.fa_ref_dequant_e4m3.argtypes = [vp, ctypes.POINTER(ctypes.c_float), L, L, L, L, dp]
+        lib.fa_ref_dequant_e4m3.restype = I
         lib.fa_ref_max_threads.argtypes = []
         lib.fa_ref_max_threads.restype = I
         _lib = lib
@@ -257,3 +261,27 @@ def _prep_like(t, ref, enc):
     if a.shape != ref.shape:
         raise ValueError("dout must have the shape of q")
     return (a,)
+
+
+def decode_e4m3(byte):
+    """Exact value of one OCP E4M3 byte (NaN for the NaN patterns)."""
+    return float(_load().fa_ref_decode_e4m3(int(byte) & 0xff))
+
+
+def dequant_e4m3(x_bytes, block_scale, block_rows=128):
+    """x_bytes [B,H,N,D] uint8 (E4M3 bit patterns), block_scale [B,H,ceil(N/block_rows)]
+    float32 -> float64 [B,H,N,D] = decode(x) * scale of the row's block."""
+    x = np.ascontiguousarray(x_bytes, dtype=np.uint8)
+    if x.ndim != 4:
+        raise ValueError("x must be [B, H, N, D]")
+    B, H, N, D = x.shape
+    nb = (N + block_rows - 1) // block_rows
+    sc = np.ascontiguousarray(block_scale, dtype=np.float32)
+    if sc.shape != (B, H, nb):
+        raise ValueError("block_scale must be [B, H, %d]" % nb)
+    out = np.empty((B, H, N, D), np.float64)
+    rc = _load().fa_ref_dequant_e4m3(x.ctypes.data, sc.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), B * H, N, D,
+                                     block_rows, _dptr(out))
+    if rc != 0:
+        raise RuntimeError("fa_ref_dequant_e4m3 failed (%d)" % rc)
+    return out
