@@ -248,9 +248,14 @@ def run_ours(args, w):
         if world > 1:
             dist.barrier()
 
-    q_h, k_h, v_h = fa_inputs.make_qkv(w, seed=args.seed + rank)
+    fp8 = args.fp8
+    if fp8:
+        # E4M3 inputs quantized per 128-row block; V handed over transposed per head
+        (q_h, k_h, v8), scales_h = fa_inputs.make_qkv_fp8(w, seed=args.seed + rank)
+        v_h = v8.transpose(2, 3).contiguous()
+        scales = [t.to(dev) for t in scales_h]
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
-    o = torch.empty_like(q)
+    o = torch.empty((w.B, w.H, w.N, w.D), dtype=torch.bfloat16, device=dev) if fp8 else torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -264,7 +269,11 @@ def run_ours(args, w):
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
     def launch(qq, kk, vv, oo, ll):
-        if splits > 0:
+        if fp8:
+            st = fa.fa_fwd_fp8(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), scales[0].data_ptr(),
+                               scales[1].data_ptr(), scales[2].data_ptr(), oo.data_ptr(), ll.data_ptr(), w.B, w.H,
+                               w.N, w.D, w.scale, int(w.causal), handle)
+        elif splits > 0:
             st = fa.fa_fwd_splitkv(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), oo.data_ptr(), ll.data_ptr(), w.B,
                                    w.H, w.N, w.D, w.scale, int(w.causal), dt, splits, ws.data_ptr(), ws_bytes,
                                    handle)
@@ -330,6 +339,10 @@ def run_ours(args, w):
     value = job_tflops(world, w.flops, ms_per_step)
     e2e_value = job_tflops(world, w.flops, e2e_ms)
     peak, hbm, peak_kind = measured_peaks()
+    peak_note = "%s dense bf16 (burst); fp16/bf16 nominal ratio 1" % peak_kind
+    if fp8:
+        peak *= 2.0   # dense FP8 runs at twice the dense bf16 rate (nominal ratio)
+        peak_note = "%s dense bf16 (burst) x 2, the nominal fp8/bf16 dense ratio" % peak_kind
     achieved = w.flops / (ms_per_step * 1e-3) / 1e12
     clk = clocks.summary()
 
@@ -337,16 +350,19 @@ def run_ours(args, w):
         "metric": "attention fwd TFLOP/s (causal-adjusted)", "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak",
-        "vs_baseline": (value / (w.flops / (PAGE_MS[w.name] * 1e-3) / 1e12)) if w.name in PAGE_MS else None,
-        "dtype": w.dtype, "data": "synthetic (seeded N(0,1) inputs, see fa_inputs.py)",
+        "vs_baseline": (value / (w.flops / (PAGE_MS[w.name] * 1e-3) / 1e12)) if (w.name in PAGE_MS and not fp8)
+        else None,
+        "dtype": "e4m3 (bf16 out)" if fp8 else w.dtype,
+        "data": "synthetic (seeded N(0,1) inputs%s, see fa_inputs.py)" % (", E4M3 per-128-row-block scales" if fp8 else ""),
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
                    "scale": w.scale, "parallelism": "replica per GPU" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (256 MiB write, outside the events)",
                    "ms_p50": statistics.median(step_ms), "ms_min": min(step_ms),
-                   "num_splits": splits, "entry": "fa_fwd_splitkv" if splits > 0 else "fa_fwd"},
+                   "num_splits": splits,
+                   "entry": "fa_fwd_fp8" if fp8 else ("fa_fwd_splitkv" if splits > 0 else "fa_fwd")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(w.name),
-                     "peak_kind": "%s dense bf16 (burst); fp16/bf16 nominal ratio 1" % peak_kind,
+                     "frac": achieved / peak, "traffic": None if fp8 else recorded_traffic(w.name),
+                     "peak_kind": peak_note,
                      "effective_GBps": w.io_bytes / (ms_per_step * 1e-3) / 1e9},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
@@ -354,7 +370,7 @@ def run_ours(args, w):
         "clocks": clk,
         "kernel_source_sha": kernel_source_hash(),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         tf, rows, secs, threads, _ = cpu_oracle_sample(w, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {
             "value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -513,6 +529,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="time fa_fwd_splitkv with this many K/V chunks per query block (0: fa_fwd)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time fa_fwd_fp8 on the workload's shape with E4M3 inputs (D = 128, N a multiple of 16)")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward pass (default, the headline) or the backward pass")
     args = ap.parse_args(argv)

@@ -58,6 +58,8 @@ def load_library():
         lib.fa_noalloc_scratch_bytes.restype = ctypes.c_size_t
         lib.fa_selftest_wait_timeout.argtypes = [vp]
         lib.fa_selftest_wait_timeout.restype = I
+        lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, vp]
+        lib.fa_fwd_fp8.restype = I
         lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, I, vp, ctypes.c_size_t, vp]
@@ -104,6 +106,13 @@ def fa_fwd_splitkv_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H: 
 
 def fa_noalloc_scratch_bytes() -> int:
     return int(load_library().fa_noalloc_scratch_bytes())
+
+
+def fa_fwd_fp8(q: int, k: int, v_t: int, q_scale: int, k_scale: int, v_scale: int, o: int, lse: int, B: int, H: int,
+               N: int, D: int, scale: float, causal: int, stream: int) -> int:
+    """Direct call of the FP8 (E4M3) forward entry point; returns its status code."""
+    return int(load_library().fa_fwd_fp8(q, k, v_t, q_scale, k_scale, v_scale, o, lse, B, H, N, D, float(scale),
+                                         int(causal), stream))
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
@@ -228,3 +237,39 @@ def attention_backward(q, k, v, out, lse, dout, causal: bool = False, scale: flo
     if st != FA_OK:
         raise FaError(st, "fa_bwd")
     return dq, dk, dv
+
+
+def attention_fp8(q8, k8, v8_t, q_scale, k_scale, v_scale, causal: bool = False, scale: float | None = None, out=None,
+                  lse=None, stream=None):
+    """O (bf16), LSE = attention of FP8 inputs: q8, k8 [B,H,N,D] and v8_t [B,H,D,N]
+    (V transposed per head) as uint8 or float8_e4m3fn CUDA tensors, with fp32
+    per-128-row block scales [B,H,ceil(N/128)].  Raises FaError on a non-OK
+    status.  Asynchronous on ``stream``."""
+    import torch
+
+    ts = (q8, k8, v8_t)
+    if not all(t.is_cuda and t.element_size() == 1 and t.is_contiguous() for t in ts):
+        raise ValueError("q8, k8, v8_t must be contiguous 1-byte CUDA tensors")
+    if q8.dim() != 4 or k8.shape != q8.shape:
+        raise ValueError("q8, k8 must be [B, H, N, D]")
+    B, H, N, D = q8.shape
+    if tuple(v8_t.shape) != (B, H, D, N):
+        raise ValueError("v8_t must be [B, H, D, N] (V transposed per head)")
+    nb = (N + 127) // 128
+    for t in (q_scale, k_scale, v_scale):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and tuple(t.shape) == (B, H, nb)):
+            raise ValueError("scales must be contiguous float32 CUDA tensors [B, H, ceil(N/128)]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q8.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8_t.data_ptr(), q_scale.data_ptr(), k_scale.data_ptr(),
+                    v_scale.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D, scale, int(bool(causal)), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_fp8")
+    return out, lse

@@ -71,14 +71,21 @@ constexpr int kRowsPerTile = kTileM * kNumQ;
 constexpr int kThreads = 128 * (2 + kNumQ);   // producer/MMA WG, softmax WGs, correction WG
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;   // 1 s per wait
 constexpr float kLazyRescale = 8.0f;          // log2 units: rescale only when the max grows > 2^8
+// FP8 path: P is stored as E4M3 (largest finite 448).  A lag of the reference
+// max of up to 2 log2 units and a range shift of 2^6 keep P <= 2^8, while
+// probabilities down to 2^-12 stay normal numbers of the format.
+constexpr float kLazyRescaleFp8 = 2.0f;
+constexpr float kFp8Shift = 6.0f;
 constexpr uint32_t kTmemCols = 512;
 
-template <int D>
+template <int D, bool FP8 = false>
 struct Cfg {
-    static constexpr int kTileBytes = kTileM * D * 2;   // one 128-row tile of Q, K or V
-    static constexpr int kBoxes = D / 64;               // 64-element (128-byte) swizzle boxes along D
+    static constexpr int kElem = FP8 ? 1 : 2;           // bytes per element of Q, K, V
+    static constexpr int kTileBytes = kTileM * D * kElem;   // one 128-row tile of Q, K or V
+    static constexpr int kBoxElems = 128 / kElem;       // elements per 128-byte swizzle row
+    static constexpr int kBoxes = D / kBoxElems;        // 128-byte swizzle boxes along D
     static constexpr int kBoxBytes = kTileM * 128;
-    static constexpr int kStages = (D == 128) ? 4 : 8;  // K/V ring slots
+    static constexpr int kStages = (D == 128 && !FP8) ? 4 : 8;  // K/V ring slots
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kNumQ * kTileBytes;
     static constexpr int kSmemBytes = kOffKV + kStages * kTileBytes + 1024;   // + 1 KB alignment slack
@@ -115,6 +122,12 @@ struct Params {
     int n_splits;        // chunks of K/V tiles per query block (1 without a split)
     int n_tiles;         // n_qblocks * BH * n_splits
     float scale_log2;    // scale * log2(e)
+    // FP8 path: per-block dequantization scales [BH][n_blocks] of Q, K and V
+    // (K and V indexed by the K/V head), 128 rows (keys) per block.
+    const float* q_scale;
+    const float* k_scale;
+    const float* v_scale;
+    int n_blocks;
 };
 
 // One work tile: query rows q0 .. q0+255 of head bh, K/V tiles j0 .. j0+n_all-1
@@ -240,10 +253,10 @@ __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, float (&s)[128])
 // ------------------------------------------------------------------ roles
 
 // K/V producer: one thread; K_j then V_j of every work tile, in order.
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool FP8>
 __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                 const Params& p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, FP8>;
     volatile int* abort_flag = &sh.abort_flag;
     prefetch_tmap(tm_k);
     prefetch_tmap(tm_v);
@@ -265,9 +278,16 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
                 }
                 mbar_arrive_expect_tx(&sh.kv_full[slot], C::kTileBytes);
                 const CUtensorMap* map = kind ? tm_v : tm_k;
-                for (int b = 0; b < C::kBoxes; ++b)
-                    tma_load_3d_hint(tiles + C::kOffKV + slot * C::kTileBytes + b * C::kBoxBytes, map,
-                                     &sh.kv_full[slot], 64 * b, (w.j0 + j) * kTileN, w.kvh, pol_keep);
+                uint8_t* dst = tiles + C::kOffKV + slot * C::kTileBytes;
+                if (FP8 && kind) {
+                    // V is stored transposed per head ([D][N], keys contiguous): one
+                    // 128-key x 128-row box, the operand K-major for the FP8 P V
+                    tma_load_3d_hint(dst, map, &sh.kv_full[slot], (w.j0 + j) * kTileN, 0, w.kvh, pol_keep);
+                } else {
+                    for (int b = 0; b < C::kBoxes; ++b)
+                        tma_load_3d_hint(dst + b * C::kBoxBytes, map, &sh.kv_full[slot], C::kBoxElems * b,
+                                         (w.j0 + j) * kTileN, w.kvh, pol_keep);
+                }
             }
         }
     }
@@ -281,9 +301,9 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
 }
 
 // Q producer: one thread; Q_t of every work tile once its buffer is free.
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool FP8>
 __device__ void run_q_producer(SharedState& sh, uint8_t* tiles, const CUtensorMap* tm_q, const Params& p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, FP8>;
     volatile int* abort_flag = &sh.abort_flag;
     prefetch_tmap(tm_q);
     const uint64_t pol_once = l2_policy_evict_first();   // Q: read once
@@ -302,8 +322,8 @@ __device__ void run_q_producer(SharedState& sh, uint8_t* tiles, const CUtensorMa
             }
             mbar_arrive_expect_tx(&sh.q_full[t], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
-                tma_load_3d_hint(tiles + C::kOffQ + t * C::kTileBytes + b * C::kBoxBytes, tm_q, &sh.q_full[t], 64 * b,
-                                 w.q0 + kTileM * t, w.bh, pol_once);
+                tma_load_3d_hint(tiles + C::kOffQ + t * C::kTileBytes + b * C::kBoxBytes, tm_q, &sh.q_full[t],
+                                 C::kBoxElems * b, w.q0 + kTileM * t, w.bh, pol_once);
             ++loads[t];
         }
     }
@@ -332,18 +352,21 @@ __device__ __forceinline__ uint32_t mbar_test3_bcast(uint64_t* b0, uint32_t p0, 
 // work tile's K_0: a stream's first S of the next tile goes out early, at the
 // end of its previous tile, and stream 0 may start only at the top of the tile
 // (when it had no K/V tiles in the previous one), after stream 1.
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8>
 __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Params& p) {
-    using C = Cfg<D>;
+    using C = Cfg<D, FP8>;
     volatile int* abort_flag = &sh.abort_flag;
-    constexpr uint32_t kIdS = idesc_f16(BF16, kTileM, kTileN, false);
-    constexpr uint32_t kIdO = idesc_f16(BF16, kTileM, D, true);
+    // FP8: kind::f8f6f4 with E4M3 operands (format code 0 in the A / B fields);
+    // P V then reads V^T K-major instead of V MN-major.
+    constexpr uint32_t kIdS = idesc_f16(FP8 ? false : BF16, kTileM, kTileN, false);
+    constexpr uint32_t kIdO = idesc_f16(FP8 ? false : BF16, kTileM, D, !FP8);
     // Descriptors are built once per operand; a K-step only moves the start
     // address field (address / 16, the low bits of the descriptor), which never
     // carries out for shared-memory addresses.
     const uint64_t dq0 = sdesc_sw128(smem_u32(tiles + C::kOffQ), 16, 1024);
     const uint64_t dkv0 = sdesc_sw128(smem_u32(tiles + C::kOffKV), 16, 1024);
-    const uint64_t dv0 = sdesc_sw128(smem_u32(tiles + C::kOffKV), C::kBoxBytes, 1024);
+    const uint64_t dv0 = FP8 ? sdesc_sw128(smem_u32(tiles + C::kOffKV), 16, 1024)
+                             : sdesc_sw128(smem_u32(tiles + C::kOffKV), C::kBoxBytes, 1024);
 
     int acquired = 0;        // ring items acquired so far
     uint32_t pv_par = 0;     // bit t: parity of stream t's next p_full phase
@@ -363,12 +386,20 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
         const uint64_t da = dq0 + ((t * C::kTileBytes) >> 4);
         const uint64_t db = dkv0 + (((item % C::kStages) * C::kTileBytes) >> 4);
         const uint32_t d = tmem + C::tm_s(t);
+        if constexpr (FP8) {
+            // K-step kk reads 32 columns of D: 32 bytes into the 128-byte row
+            umma_ss_off_elect_f8<0, 0>(d, da, db, kIdS, 0);
+            umma_ss_off_elect_f8<2, 2>(d, da, db, kIdS, 1);
+            umma_ss_off_elect_f8<4, 4>(d, da, db, kIdS, 1);
+            umma_ss_off_elect_f8<6, 6>(d, da, db, kIdS, 1);
+        } else {
         // K-step kk reads 16 columns of D: 32 bytes into a 128-byte row, in box kk / 4
         umma_ss_off_elect<0, 0>(d, da, db, kIdS, 0);
         umma_ss_off_elect<2, 2>(d, da, db, kIdS, 1);
         umma_ss_off_elect<4, 4>(d, da, db, kIdS, 1);
         umma_ss_off_elect<6, 6>(d, da, db, kIdS, 1);
-        if constexpr (D == 128) {
+        }
+        if constexpr (D == 128 && !FP8) {
             constexpr uint32_t B = C::kBoxBytes >> 4;
             umma_ss_off_elect<B + 0, B + 0>(d, da, db, kIdS, 1);
             umma_ss_off_elect<B + 2, B + 2>(d, da, db, kIdS, 1);
@@ -381,6 +412,16 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
     auto issue_pv = [&](int t, int item, bool first, bool release) {
         const uint64_t dv = dv0 + (((item % C::kStages) * C::kTileBytes) >> 4);
         const uint32_t d = tmem + C::tm_o(t), a = tmem + C::tm_s(t);
+        if constexpr (FP8) {
+            // K-step kk reads 32 keys: 8 TMEM columns of E4M3 P, 32 bytes of each V^T row
+            umma_ts_off_elect_f8<0>(d, a + 0, dv, kIdO, first ? 0u : 1u);
+            umma_ts_off_elect_f8<2>(d, a + 8, dv, kIdO, 1);
+            umma_ts_off_elect_f8<4>(d, a + 16, dv, kIdO, 1);
+            umma_ts_off_elect_f8<6>(d, a + 24, dv, kIdO, 1);
+            umma_commit_elect(&sh.pv_done[t]);
+            if (release) umma_commit_elect(&sh.kv_empty[item % C::kStages]);
+            return;
+        }
         // K-step kk reads 16 keys = 2048 bytes of V and 8 TMEM columns of P
         umma_ts_off_elect<0 * 128>(d, a + 0, dv, kIdO, first ? 0u : 1u);
         umma_ts_off_elect<1 * 128>(d, a + 8, dv, kIdO, 1);
@@ -471,8 +512,10 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
     if (!__all_sync(0xffffffffu, wait_bar(&sh.drain, 0, &never)) && lane_id() == 0) atomicOr(&g_fa_status, ST_DRAIN);
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8>
 __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params& p) {
+    static_assert(!(FP8 && SPLIT), "the FP8 path has no split-K form");
+    constexpr float kLazy = FP8 ? kLazyRescaleFp8 : kLazyRescale;
     volatile int* abort_flag = &sh.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = threadIdx.x - 128 * (1 + t);               // row of this thread in Q tile t
@@ -498,6 +541,20 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             continue;
         }
 
+        // FP8: S is the product of the E4M3 values; the scores are S times the
+        // Q and K block scales, folded into the exponent's coefficient.  P V adds
+        // E4M3 V^T bytes: each tile's V block scale, relative to the head's largest
+        // (v_ref), and a range shift of 2^6 are folded into P (see the pack below).
+        float c_q = scale_log2, v_ref = 1.f;
+        if constexpr (FP8) {
+            c_q = scale_log2 * __ldg(p.q_scale + static_cast<size_t>(w.bh) * p.n_blocks + (w.q0 + kTileM * t) / kTileM);
+            float vm = 0.f;
+            for (int b = lane; b < p.n_blocks; b += 32)
+                vm = fmaxf(vm, __ldg(p.v_scale + static_cast<size_t>(w.kvh) * p.n_blocks + b));
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, m));
+            v_ref = vm;
+        }
         float m_ref = -INFINITY;   // reference max, log2 units of the scaled score
         float l = 0.f;             // running sum of the 16-bit-rounded P actually used by P V
         float ls = 0.f;            // running sum of the unrounded p, for the log-sum-exp (bf16)
@@ -510,6 +567,14 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
 
             const int jg = SPLIT ? w.j0 + j : j;                // global K/V tile index
             const int k0 = jg * kTileN;
+            float c_s = scale_log2, shift = 0.f, fold = 1.f;   // coefficient, P shift (log2), 2^-shift
+            if constexpr (FP8) {
+                const size_t kb = static_cast<size_t>(w.kvh) * p.n_blocks + jg;
+                const float vs = __ldg(p.v_scale + kb);
+                c_s = c_q * __ldg(p.k_scale + kb);
+                shift = kFp8Shift + log2f(vs / v_ref);
+                fold = v_ref / (vs * 64.f);
+            }
             const bool need_mask = (CAUSAL && jg == (SPLIT ? w.last[t] : nkv_t - 1)) || (k0 + kTileN > N);
             if (need_mask) {
 #pragma unroll
@@ -529,13 +594,13 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
                     mx[3] = fmax3(mx[3], s[c + 6], s[c + 7]);
                 }
             }
-            const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * scale_log2;
+            const float m_tile = fmax3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) * c_s;
             const float m_new = fmaxf(m_ref, m_tile);
             float alpha = 1.f;
             if (m_ref == -INFINITY) {
                 alpha = 0.f;            // nothing accumulated yet
                 m_ref = m_new;
-            } else if (m_new > m_ref + kLazyRescale) {
+            } else if (m_new > m_ref + kLazy) {
                 alpha = ex2_approx(m_ref - m_new);
                 m_ref = m_new;
             }
@@ -557,11 +622,40 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
                 // subtracts (coefficient 1).  One loop body serves both cases: a
                 // second unrolled copy of it costs instruction-cache misses.
 #pragma unroll
-                for (int c = 0; c < kTileN; ++c) s[c] = __fmul_rn(s[c], scale_log2);
+                for (int c = 0; c < kTileN; ++c) s[c] = __fmul_rn(s[c], c_s);
             }
-            const float cf = fused ? scale_log2 : 1.f;
+            const float cf = fused ? c_s : 1.f;
             const uint64_t c2 = pack_f32x2(cf, cf);
-            const uint64_t nm2 = pack_f32x2(-msub, -msub);
+            const uint64_t nm2 = pack_f32x2(shift - msub, shift - msub);
+            if constexpr (FP8) {
+                // P'' = 2^(s c - m_ref + shift) = p * 2^6 * vs / v_ref, four per E4M3 word
+                uint64_t lx2 = pack_f32x2(0.f, 0.f);   // sum of the unrounded P''
+                uint32_t pk8[kTileN / 4];
+#pragma unroll
+                for (int i = 0; i < kTileN / 4; ++i) {
+                    float x0, x1, x2, x3;
+                    unpack_f32x2(fma_f32x2(pack_f32x2(s[4 * i], s[4 * i + 1]), c2, nm2), x0, x1);
+                    unpack_f32x2(fma_f32x2(pack_f32x2(s[4 * i + 2], s[4 * i + 3]), c2, nm2), x2, x3);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+                    pk8[i] = pack_e4m3x4(p0, p1, p2, p3);
+                    lx2 = add_f32x2(lx2, add_f32x2(pack_f32x2(p0, p1), pack_f32x2(p2, p3)));
+                }
+                tmem_st32(ts, pk8);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.p_full[t]);
+                // Row sums of the E4M3 P actually used by P V (normalises O), and of
+                // the unrounded P'' (the log-sum-exp), both back in units of p.
+                float lr[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < kTileN / 4; ++i) add_e4m3x4(pk8[i], lr[2 * (i & 1)], lr[2 * (i & 1) + 1]);
+                float x0, x1;
+                unpack_f32x2(lx2, x0, x1);
+                l = l * alpha + ((lr[0] + lr[1]) + (lr[2] + lr[3])) * fold;
+                ls = ls * alpha + (x0 + x1) * fold;
+                continue;
+            }
             uint64_t lx2 = pack_f32x2(0.f, 0.f);   // sum of the fp32 p (bf16 only)
             uint32_t pk[kTileN / 2];                 // P as packed 16-bit pairs
 #pragma unroll
@@ -634,7 +728,8 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             tc_fence_before();
             continue;
         }
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        // FP8: O holds sum P'' v8 = 2^6 / v_ref * sum p (vs v8); undo the fold
+        const float inv = l > 0.f ? (FP8 ? v_ref * 0.015625f : 1.f) / l : 0.f;
         uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + (row_ok ? row_g : 0) * D);
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
@@ -709,10 +804,11 @@ __device__ void run_correction(SharedState& sh, uint32_t tmem, const Params& p) 
     if (!ok) give_up(sh, ST_CORRECTION);
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
+    using C = Cfg<D, FP8>;
     extern __shared__ uint8_t dyn_smem[];
     __shared__ SharedState sh;
     uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
@@ -727,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.alpha_ready[t], 4);
             mbar_init(&sh.pv_done[t], 1);
         }
-        for (int s = 0; s < Cfg<D>::kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&sh.kv_full[s], 1);
             mbar_init(&sh.kv_empty[s], 1);
         }
@@ -747,15 +843,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (wg == 0) {
         setmaxnreg_dec<96>();
         if (warp == 0 && lane == 0)
-            run_kv_producer<D, CAUSAL, SPLIT>(sh, tiles, &tm_k, &tm_v, p);
+            run_kv_producer<D, CAUSAL, SPLIT, FP8>(sh, tiles, &tm_k, &tm_v, p);
         else if (warp == 1)
-            run_mma<D, BF16, CAUSAL, SPLIT>(sh, tiles, tmem, p);
+            run_mma<D, BF16, CAUSAL, SPLIT, FP8>(sh, tiles, tmem, p);
         else if (warp == 2 && lane == 0)
-            run_q_producer<D, CAUSAL, SPLIT>(sh, tiles, &tm_q, p);
+            run_q_producer<D, CAUSAL, SPLIT, FP8>(sh, tiles, &tm_q, p);
         __syncwarp();
     } else if (wg <= kNumQ) {
         setmaxnreg_inc<176>();
-        run_softmax<D, BF16, CAUSAL, SPLIT>(sh, tmem, wg - 1, p);
+        run_softmax<D, BF16, CAUSAL, SPLIT, FP8>(sh, tmem, wg - 1, p);
     } else {
         setmaxnreg_dec<64>();
         run_correction<D, CAUSAL, SPLIT>(sh, tmem, p);
@@ -834,24 +930,24 @@ __global__ void __launch_bounds__(32) selftest_wait_timeout_kernel() {
 
 // ------------------------------------------------------------------ host
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8 = false>
 static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
                           cudaStream_t stream) {
-    auto kern = fa_fwd_kernel<D, BF16, CAUSAL, SPLIT>;
+    auto kern = fa_fwd_kernel<D, BF16, CAUSAL, SPLIT, FP8>;
     static std::atomic<uint64_t> configured{0};   // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
     if (!bit || !(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, FP8>::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
     const int sms = sm_count(dev);
     if (sms <= 0) return cudaErrorInvalidDevice;
     const unsigned grid = static_cast<unsigned>(p.n_tiles < sms ? p.n_tiles : sms);
-    kern<<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(q, k, v, p);
+    kern<<<grid, kThreads, Cfg<D, FP8>::kSmemBytes, stream>>>(q, k, v, p);
     return cudaGetLastError();
 }
 
@@ -903,6 +999,8 @@ static int prepare(const void* q, const void* k, const void* v, void* o, float* 
     p.n_splits = n_splits;
     p.n_tiles = static_cast<int>(n_qblocks * BH * static_cast<uint64_t>(n_splits));
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.q_scale = p.k_scale = p.v_scale = nullptr;
+    p.n_blocks = 0;
     return FA_OK;
 }
 
@@ -993,6 +1091,77 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
     st = dispatch<true>(maps, p, D, dtype, causal, stream);
     if (st != FA_OK) return st;
     return dispatch_merge(p, D, dtype, stream);
+}
+
+// ------------------------------------------------------------------ FP8 forward
+namespace fa103 {
+
+// [BH, rows, inner] view of a contiguous byte tensor: 128-byte x 128-row boxes,
+// 128-byte swizzle.  `inner` must make the row stride a multiple of 16 bytes.
+static bool make_byte_map(CUtensorMap* map, const void* base, int inner, int rows, int BH) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows) * inner};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t elem_strides[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, elem_strides,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace fa103
+
+extern "C" int fa_fwd_fp8(const void* q, const void* k, const void* v_t, const float* q_scale, const float* k_scale,
+                          const float* v_scale, void* o, float* lse, int B, int H, int N, int D, float scale,
+                          int causal, cudaStream_t stream) {
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (D != 128) return FA_ERR_UNSUPPORTED;
+    if (N % 16 != 0) return FA_ERR_INVALID_ARG;   // V^T rows of N bytes: TMA strides are multiples of 16 bytes
+    const void* ptrs[8] = {q, k, v_t, q_scale, k_scale, v_scale, o, lse};
+    for (const void* ptr : ptrs)
+        if (ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return FA_ERR_MISALIGNED;
+    const uint64_t BH = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
+    const uint64_t elems = BH * static_cast<uint64_t>(N) * static_cast<uint64_t>(D);
+    if (BH > 0x7fffffffull || elems >= (uint64_t(1) << 40)) return FA_ERR_INVALID_ARG;
+    const uint64_t n_qblocks = (static_cast<uint64_t>(N) + kRowsPerTile - 1) / kRowsPerTile;
+    if (n_qblocks * BH > 0x7fffffffull) return FA_ERR_INVALID_ARG;
+    const int n_blocks = (N + kTileN - 1) / kTileN;
+    const size_t in_bytes = static_cast<size_t>(elems), sc_bytes = static_cast<size_t>(BH) * n_blocks * 4;
+    const size_t o_bytes = static_cast<size_t>(elems) * 2, l_bytes = static_cast<size_t>(BH) * N * 4;
+    const void* ins[6] = {q, k, v_t, q_scale, k_scale, v_scale};
+    const size_t ib[6] = {in_bytes, in_bytes, in_bytes, sc_bytes, sc_bytes, sc_bytes};
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(o, o_bytes, ins[i], ib[i]) || overlaps(lse, l_bytes, ins[i], ib[i])) return FA_ERR_INVALID_ARG;
+    if (overlaps(o, o_bytes, lse, l_bytes)) return FA_ERR_INVALID_ARG;
+    CUtensorMap maps[3];
+    const int bh = static_cast<int>(BH);
+    if (!make_byte_map(&maps[0], q, D, N, bh) || !make_byte_map(&maps[1], k, D, N, bh) ||
+        !make_byte_map(&maps[2], v_t, N, D, bh))
+        return FA_ERR_CUDA;
+    Params p;
+    p.o = o;
+    p.lse = lse;
+    p.ws_o = nullptr;
+    p.ws_st = nullptr;
+    p.N = N;
+    p.BH = bh;
+    p.H = H;
+    p.kv_group = 1;
+    p.n_qblocks = static_cast<int>(n_qblocks);
+    p.n_splits = 1;
+    p.n_tiles = static_cast<int>(n_qblocks * BH);
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.q_scale = q_scale;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
+    p.n_blocks = n_blocks;
+    const cudaError_t e = causal ? launch<128, true, true, false, true>(maps[0], maps[1], maps[2], p, stream)
+                                 : launch<128, true, false, false, true>(maps[0], maps[1], maps[2], p, stream);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ no-allocation split-K

@@ -222,6 +222,32 @@ __device__ __forceinline__ void umma_ts_off_elect(uint32_t d_tmem, uint32_t a_tm
         "r"(a_tmem), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_B)
         : "memory");
 }
+// kind::f8f6f4 forms (8-bit operands, K = 32 per instruction), elected lane.
+template <uint32_t OFF_A, uint32_t OFF_B>
+__device__ __forceinline__ void umma_ss_off_elect_f8(uint32_t d_tmem, uint64_t a_base, uint64_t b_base, uint32_t idesc,
+                                                     uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 a, b;\n\t"
+        "add.s64 a, %1, %5;\n\t"
+        "add.s64 b, %2, %6;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_A), "n"(OFF_B)
+        : "memory");
+}
+template <uint32_t OFF_B>
+__device__ __forceinline__ void umma_ts_off_elect_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_base, uint32_t idesc,
+                                                     uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t.reg .b64 b;\n\t"
+        "add.s64 b, %2, %5;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], b, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_B)
+        : "memory");
+}
 __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -397,6 +423,36 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Four fp32 values to OCP E4M3 bytes (round to nearest even, saturating to
+// +-448), a in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+// The four E4M3 bytes of w added exactly into two fp32 accumulators
+// (bytes 0 and 2 into acc0, bytes 1 and 3 into acc1): each pair of bytes is
+// widened to f16x2 (exact) and each half added with one rounding to fp32.
+__device__ __forceinline__ void add_e4m3x4(uint32_t w, float& acc0, float& acc1) {
+    asm("{\n\t.reg .b16 lo, hi, h0, h1, h2, h3;\n\t.reg .b32 f01, f23;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 f01, lo;\n\t"
+        "cvt.rn.f16x2.e4m3x2 f23, hi;\n\t"
+        "mov.b32 {h0, h1}, f01;\n\t"
+        "mov.b32 {h2, h3}, f23;\n\t"
+        "add.rn.f32.f16 %0, h0, %0;\n\t"
+        "add.rn.f32.f16 %1, h1, %1;\n\t"
+        "add.rn.f32.f16 %0, h2, %0;\n\t"
+        "add.rn.f32.f16 %1, h3, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(w));
 }
 
 // Three-input max.

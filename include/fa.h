@@ -151,6 +151,37 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
 size_t fa_noalloc_scratch_bytes(void);
 
 /*
+ * fa_fwd_fp8 -- the forward pass on 8-bit inputs ("CUDA FlashAttention: from
+ * online softmax to the long-sequence IO limit", section 2: FP8 Q/K/V need a
+ * per-tensor or per-block scale, and the softmax state stays FP32).
+ *
+ *   q, k       [B,H,N,D] OCP E4M3 bytes                         (device, read)
+ *   v_t        V transposed per head: [B,H,D,N] E4M3 bytes, keys contiguous
+ *              (both operands of the FP8 tensor-core product P V are read
+ *              K-major)                                          (device, read)
+ *   q_scale, k_scale, v_scale
+ *              [B,H,ceil(N/128)] fp32 dequantization scales: element x of
+ *              rows (keys) 128*b .. 128*b+127 of head (b, h) stands for
+ *              E4M3(x) * scale[b, h, block]; positive and finite  (device, read)
+ *   o          [B,H,N,D] bf16 output                              (device, written)
+ *   lse        [B,H,N] fp32 natural-log LSE of the dequantized scores (device, written)
+ *   B, H, N, scale, causal, stream   as for fa_fwd; D must be 128
+ *              (else FA_ERR_UNSUPPORTED) and N a multiple of 16 (else
+ *              FA_ERR_INVALID_ARG: the rows of v_t are N bytes long and the
+ *              tensor-copy engine needs 16-byte strides)
+ *
+ * S = Q K^T runs on 8-bit operands with FP32 accumulation and is scaled by the
+ * two block scales; the running max, the sums and O stay FP32.  P enters the
+ * FP8 product P V as E4M3, carrying a power-of-two range shift and the ratio of
+ * its V block's scale to the head's largest V block scale; O is normalised by
+ * the sum of those E4M3 P values (an exact convex combination of dequantized V
+ * rows), the LSE uses the unrounded sum.  Errors and codes as for fa_fwd.
+ */
+int fa_fwd_fp8(const void* q, const void* k, const void* v_t, const float* q_scale, const float* k_scale,
+               const float* v_scale, void* o, float* lse, int B, int H, int N, int D, float scale, int causal,
+               cudaStream_t stream);
+
+/*
  * fa_bwd_workspace_bytes -- bytes of workspace fa_bwd needs for these sizes:
  * an fp32 dQ accumulator (4*B*H*N*D bytes) and one fp32 value per query row
  * (4*B*H*N), each rounded up to 256 bytes.  Returns 0 for invalid sizes (any

@@ -140,3 +140,25 @@ def test_bwd_binding_rejects_bad_tensors(lib):
     lse = torch.zeros(1, 1, 8)
     with pytest.raises(ValueError):
         fa.attention_backward(x, x, x, x, lse, x)
+
+
+FP8 = dict(q=1 << 20, k=2 << 20, vt=3 << 20, qs=4 << 20, ks=5 << 20, vs=6 << 20, o=7 << 20, lse=8 << 20,
+           B=1, H=2, N=256, D=128, scale=0.09, causal=1)
+
+
+def _fp8(**kw):
+    a = dict(FP8, **kw)
+    return fa.fa_fwd_fp8(a["q"], a["k"], a["vt"], a["qs"], a["ks"], a["vs"], a["o"], a["lse"], a["B"], a["H"],
+                         a["N"], a["D"], a["scale"], a["causal"], 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=64), 2), (dict(D=96), 2),
+    (dict(N=100), 1), (dict(N=0), 1), (dict(B=0), 1), (dict(causal=3), 1), (dict(scale=-1.0), 1),
+    (dict(q=0), 3), (dict(vs=0), 3), (dict(ks=(5 << 20) + 4), 3), (dict(lse=(8 << 20) + 8), 3),
+    (dict(o=(1 << 20) + 4096), 1),            # o overlaps q
+    (dict(lse=(7 << 20) + 1024), 1),          # lse overlaps o
+    (dict(o=(4 << 20) - 64 * 1024), 1),       # o overlaps the Q scales
+])
+def test_fp8_argument_errors_without_gpu(lib, kw, status):
+    assert _fp8(**kw) == status
