@@ -686,3 +686,55 @@ int fa_ref_dequant_e4m3(const uint8_t* x, const float* block_scale, long BH, lon
         }
     return 0;
 }
+
+/* ---- queries against a longer key/value sequence ------------------------- */
+
+int fa_ref_naive_kv(const void* q, const void* k, const void* v, int enc, double* o, double* lse, long B, long H,
+                    long H_kv, long Nq, long Nk, long D, double scale, int causal, int nthreads)
+{
+    if (bad_args(q, k, v, enc, B, H, Nq, D) || !o || !lse || Nk < 1 || H_kv < 1 || H % H_kv != 0) return -1;
+    if (causal && Nq > Nk) return -1;
+    set_threads(nthreads);
+    const long group = H / H_kv;
+    int err = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)Nk);
+        if (!s) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 16)
+            for (long r = 0; r < B * H * Nq; ++r) {
+                long bh = r / Nq, i = r - bh * Nq;
+                long b = bh / H, h = bh - b * H;
+                size_t q_base = (size_t)bh * (size_t)Nq * (size_t)D;
+                size_t kv_base = ((size_t)b * (size_t)H_kv + (size_t)(h / group)) * (size_t)Nk * (size_t)D;
+                /* query i sits at position i + Nk - Nq of the key sequence */
+                long nvis = causal ? i + (Nk - Nq) + 1 : Nk;
+                double* orow = o + (size_t)r * (size_t)D;
+                size_t qrow = q_base + (size_t)i * (size_t)D;
+                double m = -INFINITY;
+                for (long j = 0; j < nvis; ++j) {
+                    size_t krow = kv_base + (size_t)j * (size_t)D;
+                    double dot = 0.0;
+                    for (long d = 0; d < D; ++d) dot += load(q, enc, qrow + d) * load(k, enc, krow + d);
+                    s[j] = scale * dot;
+                    if (s[j] > m) m = s[j];
+                }
+                for (long d = 0; d < D; ++d) orow[d] = 0.0;
+                double l = 0.0;
+                for (long j = 0; j < nvis; ++j) {
+                    double p = exp(s[j] - m);
+                    size_t vrow = kv_base + (size_t)j * (size_t)D;
+                    l += p;
+                    for (long d = 0; d < D; ++d) orow[d] += p * load(v, enc, vrow + d);
+                }
+                for (long d = 0; d < D; ++d) orow[d] /= l;
+                lse[r] = m + log(l);
+            }
+        }
+        free(s);
+    }
+    return err ? -2 : 0;
+}

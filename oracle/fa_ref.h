@@ -134,6 +134,16 @@ int fa_ref_backward_sample(const void* q, const void* k, const void* v, const vo
                            const long* kv_bh, const long* kv_keys, long n_kv, double* dk_out, double* dv_out,
                            int nthreads);
 
+/* Nq queries against Nk >= Nq keys ("CUDA FlashAttention: from online softmax
+ * to the long-sequence IO limit", section 7: split-KV / flash-decoding, where
+ * one or a few new queries attend to a long key/value sequence), with grouped
+ * K/V heads: q [B, H, Nq, D], k, v [B, H_kv, Nk, D], o [B, H, Nq, D], lse
+ * [B, H, Nq].  Query i is the token at position i + Nk - Nq of the sequence,
+ * so with `causal` it sees keys j <= i + Nk - Nq (Nq = Nk gives the square
+ * mask above; Nq = 1 sees every key).  Otherwise the naive definition. */
+int fa_ref_naive_kv(const void* q, const void* k, const void* v, int enc, double* o, double* lse, long B, long H,
+                    long H_kv, long Nq, long Nk, long D, double scale, int causal, int nthreads);
+
 /* FP8 inputs ("CUDA FlashAttention: from online softmax to the long-sequence
  * IO limit", section 2: 8-bit Q/K/V need a per-tensor or per-block scale; the
  * softmax state stays FP32).  fa_ref_decode_e4m3 decodes one OCP E4M3 byte

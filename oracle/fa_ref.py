@@ -64,6 +64,8 @@ def _load():
         lib.fa_ref_backward_sample.argtypes = [vp, vp, vp, vp, I, L, L, L, L, Dbl, I, lp, lp, L, dp,
                                                lp, lp, L, dp, dp, I]
         lib.fa_ref_backward_sample.restype = I
+        lib.fa_ref_naive_kv.argtypes = [vp, vp, vp, I, dp, dp, L, L, L, L, L, L, Dbl, I, I]
+        lib.fa_ref_naive_kv.restype = I
         lib.fa_ref_decode_e4m3.argtypes = [ctypes.c_uint8]
         lib.fa_ref_decode_e4m3.restype = Dbl
         lib.fa_ref_dequant_e4m3.argtypes = [vp, ctypes.POINTER(ctypes.c_float), L, L, L, L, dp]
@@ -285,3 +287,24 @@ def dequant_e4m3(x_bytes, block_scale, block_rows=128):
     if rc != 0:
         raise RuntimeError("fa_ref_dequant_e4m3 failed (%d)" % rc)
     return out
+
+
+def naive_kv(q, k, v, scale, causal=False, enc="f64", nthreads=0):
+    """q [B,H,Nq,D] against k, v [B,H_kv,Nk,D] (Nk >= Nq when causal; query i is
+    sequence position i + Nk - Nq).  Returns (O [B,H,Nq,D], LSE [B,H,Nq])."""
+    want = np.float64 if enc == "f64" else np.uint16
+    q, k, v = (np.ascontiguousarray(t) for t in (q, k, v))
+    for t in (q, k, v):
+        if t.dtype != want or t.ndim != 4:
+            raise TypeError("enc=%s needs 4-D %s arrays" % (enc, np.dtype(want)))
+    B, H, Nq, D = q.shape
+    H_kv, Nk = k.shape[1], k.shape[2]
+    if k.shape != (B, H_kv, Nk, D) or v.shape != k.shape:
+        raise ValueError("k, v must be [B, H_kv, Nk, D]")
+    o = np.empty((B, H, Nq, D), np.float64)
+    lse = np.empty((B, H, Nq), np.float64)
+    rc = _load().fa_ref_naive_kv(q.ctypes.data, k.ctypes.data, v.ctypes.data, ENC[enc], _dptr(o), _dptr(lse),
+                                 B, H, H_kv, Nq, Nk, D, float(scale), int(bool(causal)), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("fa_ref_naive_kv failed (%d)" % rc)
+    return o, lse
