@@ -58,6 +58,10 @@ def load_library():
         lib.fa_noalloc_scratch_bytes.restype = ctypes.c_size_t
         lib.fa_selftest_wait_timeout.argtypes = [vp]
         lib.fa_selftest_wait_timeout.restype = I
+        lib.fa_fwd_kv_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.fa_fwd_kv_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, I, F, I, I, I, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_kv.restype = I
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, vp]
         lib.fa_fwd_fp8.restype = I
         lib.fa_bwd_workspace_bytes.argtypes = [I, I, I, I]
@@ -106,6 +110,18 @@ def fa_fwd_splitkv_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H: 
 
 def fa_noalloc_scratch_bytes() -> int:
     return int(load_library().fa_noalloc_scratch_bytes())
+
+
+def fa_fwd_kv_workspace_bytes(B: int, H: int, Nq: int, D: int, num_splits: int) -> int:
+    return int(load_library().fa_fwd_kv_workspace_bytes(B, H, Nq, D, num_splits))
+
+
+def fa_fwd_kv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, H_kv: int, Nq: int, Nk: int, D: int,
+              scale: float, causal: int, dtype: int, num_splits: int, workspace: int, workspace_bytes: int,
+              stream: int) -> int:
+    """Direct call of the queries-against-a-K/V-sequence entry point; returns its status code."""
+    return int(load_library().fa_fwd_kv(q, k, v, o, lse, B, H, H_kv, Nq, Nk, D, float(scale), int(causal),
+                                        int(dtype), int(num_splits), workspace, int(workspace_bytes), stream))
 
 
 def fa_fwd_fp8(q: int, k: int, v_t: int, q_scale: int, k_scale: int, v_scale: int, o: int, lse: int, B: int, H: int,
@@ -272,4 +288,42 @@ def attention_fp8(q8, k8, v8_t, q_scale, k_scale, v_scale, causal: bool = False,
                     v_scale.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D, scale, int(bool(causal)), handle)
     if st != FA_OK:
         raise FaError(st, "fa_fwd_fp8")
+    return out, lse
+
+
+def attention_kv(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 0, out=None, lse=None,
+                 workspace=None, stream=None):
+    """O, LSE for q [B,H,Nq,D] against k, v [B,H_kv,Nk,D] (fp16/bf16 CUDA tensors;
+    query i is the token at position i + Nk - Nq).  ``num_splits`` > 0 selects
+    split-K with a torch-allocated workspace unless one is given."""
+    import torch
+
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, float16 or bfloat16")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape or k.shape[0] != q.shape[0] or k.shape[3] != q.shape[3]:
+        raise ValueError("q must be [B, H, Nq, D] and k, v [B, H_kv, Nk, D]")
+    if not all(t.is_contiguous() for t in (q, k, v)):
+        raise ValueError("q, k, v must be contiguous")
+    B, H, Nq, D = q.shape
+    H_kv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    ws_ptr, ws_bytes = 0, 0
+    if num_splits > 0:
+        need = fa_fwd_kv_workspace_bytes(B, H, Nq, D, num_splits)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    dt = FA_BF16 if q.dtype == torch.bfloat16 else FA_FP16
+    st = fa_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, H_kv, Nq, Nk, D,
+                   scale, int(bool(causal)), dt, num_splits, ws_ptr, ws_bytes, handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_kv")
     return out, lse

@@ -114,7 +114,11 @@ struct Params {
     float* lse;
     float* ws_o;         // split mode: partial O, [splits][BH][N][D] fp32 (null otherwise)
     float4* ws_st;       // split mode: partial (m, l, l_exact, -), [splits][BH][N]
-    int N;
+    int N;               // query rows of a Q plane (the sequence length for square attention)
+    int Nk;              // keys of a K/V plane
+    int q_per;           // query positions per head (rows of a plane are q_per x heads when packed)
+    int causal_off;      // Nk - q_per: query position i is the token at i + causal_off
+    int packed;          // 1: a Q plane stacks the query heads that share one K/V head
     int BH;
     int H;               // query heads per batch entry
     int kv_group;        // query heads per K/V head (1 without grouped K/V heads)
@@ -135,7 +139,6 @@ struct Params {
 struct Tile {
     int q0, bh, kvh, split, j0, n_all;   // kvh: K/V plane b * H_kv + h / kv_group
     int nkv[kNumQ];      // K/V tiles of this chunk each stream visits (0: none)
-    int last[kNumQ];     // global index of each stream's last K/V tile (its causal diagonal)
 };
 
 template <bool CAUSAL, bool SPLIT>
@@ -151,12 +154,15 @@ __device__ __forceinline__ Tile make_tile(const Params& p, int idx) {
 #pragma unroll
     for (int t = 0; t < kNumQ; ++t) {
         const int r0 = w.q0 + kTileM * t;
-        if (r0 >= p.N)
+        if (r0 >= p.N) {
             full[t] = 0;
-        else if (CAUSAL)
-            full[t] = min(r0 + kTileM - 1, p.N - 1) / kTileN + 1;
-        else
-            full[t] = (p.N + kTileN - 1) / kTileN;
+        } else if (CAUSAL) {
+            // the last key any row of this Q tile sees: that of its last position
+            const int qlast = p.packed ? p.q_per - 1 : min(r0 + kTileM - 1, p.N - 1);
+            full[t] = min(qlast + p.causal_off, p.Nk - 1) / kTileN + 1;
+        } else {
+            full[t] = (p.Nk + kTileN - 1) / kTileN;
+        }
         full_all = max(full_all, full[t]);
     }
     // chunk `split` of the query block's K/V range [0, full_all)
@@ -167,7 +173,6 @@ __device__ __forceinline__ Tile make_tile(const Params& p, int idx) {
 #pragma unroll
     for (int t = 0; t < kNumQ; ++t) {
         w.nkv[t] = max(0, min(j1, full[t]) - w.j0);
-        w.last[t] = full[t] - 1;
         w.n_all = max(w.n_all, w.nkv[t]);
     }
     return w;
@@ -532,7 +537,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
         if (idx < 0) break;
         const Tile w = make_tile<CAUSAL, SPLIT>(p, idx);
         const int nkv_t = w.nkv[t];
-        const int qi = w.q0 + kTileM * t + r;                 // global query index of this row
+        const int qi = w.q0 + kTileM * t + r;                 // row of this thread in its Q plane
         const size_t row_g = static_cast<size_t>(w.bh) * N + qi;
         if (nkv_t == 0) {
             // split mode: this chunk holds none of the stream's keys
@@ -575,12 +580,20 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
                 shift = kFp8Shift + log2f(vs / v_ref);
                 fold = v_ref / (vs * 64.f);
             }
-            const bool need_mask = (CAUSAL && jg == (SPLIT ? w.last[t] : nkv_t - 1)) || (k0 + kTileN > N);
+            // Causal: the row's query is the token at position qpos of the key
+            // sequence (qi + Nk - Nq; with stacked heads, its position within its
+            // head).  A tile needs the element mask if it holds a key past the
+            // smallest position of the stream's rows, or keys past Nk.  (Read from
+            // the kernel parameters here, not kept live across the loop.)
+            const bool need_mask = (CAUSAL && k0 + kTileN - 1 > (p.packed ? 0 : w.q0 + kTileM * t) + p.causal_off) ||
+                                   (k0 + kTileN > p.Nk);
             if (need_mask) {
+                const int qpos = (p.packed ? qi % p.q_per : qi) + p.causal_off;
+                const int Nk = p.Nk;
 #pragma unroll
                 for (int c = 0; c < kTileN; ++c) {
                     const int key = k0 + c;
-                    if (key >= N || (CAUSAL && key > qi)) s[c] = -INFINITY;
+                    if (key >= Nk || (CAUSAL && key > qpos)) s[c] = -INFINITY;
                 }
             }
             // Row max of the raw scores (three-input max), then into log2 units.
@@ -957,12 +970,18 @@ using namespace fa103;
 
 namespace fa103 {
 
-// Argument checks and kernel parameters shared by both forward entry points.
-static int prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int N,
-                   int D, float scale, int causal, int dtype, int n_splits, CUtensorMap (&maps)[3], Params& p) {
-    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+// Argument checks and kernel parameters shared by the 16-bit forward entry
+// points.  Q, O, LSE have Nq rows per head, K and V Nk rows per K/V head.  With
+// `pack`, the query heads that share a K/V head are stacked into one Q plane of
+// (H / H_kv) * Nq rows (their rows are adjacent in memory), so one K/V head is
+// streamed once for all of them.
+static int prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int Nq,
+                   int Nk, int D, float scale, int causal, int dtype, int n_splits, bool pack, CUtensorMap (&maps)[3],
+                   Params& p) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
     if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (causal && Nq > Nk) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
@@ -970,12 +989,18 @@ static int prepare(const void* q, const void* k, const void* v, void* o, float* 
     for (const void* ptr : ptrs)
         if (ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return FA_ERR_MISALIGNED;
     const uint64_t BH = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
-    const uint64_t elems = BH * static_cast<uint64_t>(N) * static_cast<uint64_t>(D);
-    if (BH > 0x7fffffffull || elems >= (uint64_t(1) << 40)) return FA_ERR_INVALID_ARG;
-    const uint64_t n_qblocks = (static_cast<uint64_t>(N) + kRowsPerTile - 1) / kRowsPerTile;
-    if (n_qblocks * BH * static_cast<uint64_t>(n_splits) > 0x7fffffffull) return FA_ERR_INVALID_ARG;
-    const size_t tbytes = static_cast<size_t>(elems) * 2, lbytes = static_cast<size_t>(BH) * N * sizeof(float);
-    const size_t kvbytes = tbytes / static_cast<size_t>(H / H_kv);
+    const uint64_t BHkv = static_cast<uint64_t>(B) * static_cast<uint64_t>(H_kv);
+    const uint64_t q_elems = BH * static_cast<uint64_t>(Nq) * static_cast<uint64_t>(D);
+    const uint64_t kv_elems = BHkv * static_cast<uint64_t>(Nk) * static_cast<uint64_t>(D);
+    if (BH > 0x7fffffffull || q_elems >= (uint64_t(1) << 40) || kv_elems >= (uint64_t(1) << 40))
+        return FA_ERR_INVALID_ARG;
+    const uint64_t planes = pack ? BHkv : BH;
+    const uint64_t rows = pack ? static_cast<uint64_t>(H / H_kv) * Nq : static_cast<uint64_t>(Nq);
+    if (rows > 0x7fffffffull) return FA_ERR_INVALID_ARG;
+    const uint64_t n_qblocks = (rows + kRowsPerTile - 1) / kRowsPerTile;
+    if (n_qblocks * planes * static_cast<uint64_t>(n_splits) > 0x7fffffffull) return FA_ERR_INVALID_ARG;
+    const size_t tbytes = static_cast<size_t>(q_elems) * 2, lbytes = static_cast<size_t>(BH) * Nq * sizeof(float);
+    const size_t kvbytes = static_cast<size_t>(kv_elems) * 2;
     const void* ins[3] = {q, k, v};
     const size_t in_bytes[3] = {tbytes, kvbytes, kvbytes};
     for (int i = 0; i < 3; ++i)
@@ -983,21 +1008,25 @@ static int prepare(const void* q, const void* k, const void* v, void* o, float* 
             return FA_ERR_INVALID_ARG;
     if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
 
-    const int bh = static_cast<int>(BH), bhkv = B * H_kv;
-    if (!make_tile_map(&maps[0], q, dtype, D, N, bh) || !make_tile_map(&maps[1], k, dtype, D, N, bhkv) ||
-        !make_tile_map(&maps[2], v, dtype, D, N, bhkv))
+    if (!make_tile_map(&maps[0], q, dtype, D, static_cast<int>(rows), static_cast<int>(planes)) ||
+        !make_tile_map(&maps[1], k, dtype, D, Nk, static_cast<int>(BHkv)) ||
+        !make_tile_map(&maps[2], v, dtype, D, Nk, static_cast<int>(BHkv)))
         return FA_ERR_CUDA;
     p.o = o;
     p.lse = lse;
     p.ws_o = nullptr;
     p.ws_st = nullptr;
-    p.N = N;
-    p.BH = bh;
-    p.H = H;
-    p.kv_group = H / H_kv;
+    p.N = static_cast<int>(rows);
+    p.Nk = Nk;
+    p.q_per = Nq;
+    p.causal_off = Nk - Nq;
+    p.packed = pack ? 1 : 0;
+    p.BH = static_cast<int>(planes);
+    p.H = pack ? H_kv : H;
+    p.kv_group = pack ? 1 : H / H_kv;
     p.n_qblocks = static_cast<int>(n_qblocks);
     p.n_splits = n_splits;
-    p.n_tiles = static_cast<int>(n_qblocks * BH * static_cast<uint64_t>(n_splits));
+    p.n_tiles = static_cast<int>(n_qblocks * planes * static_cast<uint64_t>(n_splits));
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.q_scale = p.k_scale = p.v_scale = nullptr;
     p.n_blocks = 0;
@@ -1046,7 +1075,7 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
                       float scale, int causal, int dtype, cudaStream_t stream) {
     CUtensorMap maps[3];
     Params p;
-    const int st = prepare(q, k, v, o, lse, B, H, H, N, D, scale, causal, dtype, 1, maps, p);
+    const int st = prepare(q, k, v, o, lse, B, H, H, N, N, D, scale, causal, dtype, 1, false, maps, p);
     if (st != FA_OK) return st;
     return dispatch<false>(maps, p, D, dtype, causal, stream);
 }
@@ -1055,7 +1084,7 @@ extern "C" int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, 
                           int N, int D, float scale, int causal, int dtype, cudaStream_t stream) {
     CUtensorMap maps[3];
     Params p;
-    const int st = prepare(q, k, v, o, lse, B, H, H_kv, N, D, scale, causal, dtype, 1, maps, p);
+    const int st = prepare(q, k, v, o, lse, B, H, H_kv, N, N, D, scale, causal, dtype, 1, false, maps, p);
     if (st != FA_OK) return st;
     return dispatch<false>(maps, p, D, dtype, causal, stream);
 }
@@ -1082,9 +1111,49 @@ extern "C" int fa_fwd_splitkv(const void* q, const void* k, const void* v, void*
     }
     CUtensorMap maps[3];
     Params p;
-    int st = prepare(q, k, v, o, lse, B, H, H, N, D, scale, causal, dtype, num_splits, maps, p);
+    int st = prepare(q, k, v, o, lse, B, H, H, N, N, D, scale, causal, dtype, num_splits, false, maps, p);
     if (st != FA_OK) return st;
     const long long rows = static_cast<long long>(p.BH) * N;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_st = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) +
+                                        static_cast<size_t>(num_splits) * rows * D * 4);
+    st = dispatch<true>(maps, p, D, dtype, causal, stream);
+    if (st != FA_OK) return st;
+    return dispatch_merge(p, D, dtype, stream);
+}
+
+// ------------------------------------------------------------------ queries against a K/V sequence
+extern "C" size_t fa_fwd_kv_workspace_bytes(int B, int H, int Nq, int D, int num_splits) {
+    return fa_splitkv_workspace_bytes(B, H, Nq, D, num_splits);
+}
+
+extern "C" int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
+                         int Nq, int Nk, int D, float scale, int causal, int dtype, int num_splits, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
+    if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+    const int n_splits = num_splits > 0 ? num_splits : 1;
+    if (num_splits > 0) {
+        const size_t need = fa_fwd_kv_workspace_bytes(B, H, Nq, D, num_splits);
+        if (need != 0) {   // sizes valid: check the workspace before anything touches CUDA
+            if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0) return FA_ERR_MISALIGNED;
+            if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+            const size_t qb = static_cast<size_t>(B) * H * Nq * D * 2, lb = static_cast<size_t>(B) * H * Nq * 4;
+            const size_t kvb = H_kv > 0 ? static_cast<size_t>(B) * H_kv * Nk * D * 2 : 0;
+            const void* others[4] = {q, k, v, o};
+            const size_t ob[4] = {qb, kvb, kvb, qb};
+            for (int i = 0; i < 4; ++i)
+                if (others[i] != nullptr && overlaps(workspace, need, others[i], ob[i])) return FA_ERR_INVALID_ARG;
+            if (lse != nullptr && overlaps(workspace, need, lse, lb)) return FA_ERR_INVALID_ARG;
+        }
+    }
+    // Few query rows per head (decode): stack the heads of a K/V group into one Q plane.
+    const bool pack = H_kv > 0 && H % H_kv == 0 && H_kv < H && Nq < kTileM;
+    CUtensorMap maps[3];
+    Params p;
+    int st = prepare(q, k, v, o, lse, B, H, H_kv, Nq, Nk, D, scale, causal, dtype, n_splits, pack, maps, p);
+    if (st != FA_OK) return st;
+    if (num_splits == 0) return dispatch<false>(maps, p, D, dtype, causal, stream);
+    const long long rows = static_cast<long long>(p.BH) * p.N;
     p.ws_o = static_cast<float*>(workspace);
     p.ws_st = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) +
                                         static_cast<size_t>(num_splits) * rows * D * 4);
@@ -1148,6 +1217,10 @@ extern "C" int fa_fwd_fp8(const void* q, const void* k, const void* v_t, const f
     p.ws_o = nullptr;
     p.ws_st = nullptr;
     p.N = N;
+    p.Nk = N;
+    p.q_per = N;
+    p.causal_off = 0;
+    p.packed = 0;
     p.BH = bh;
     p.H = H;
     p.kv_group = 1;

@@ -151,6 +151,33 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
 size_t fa_noalloc_scratch_bytes(void);
 
 /*
+ * fa_fwd_kv -- Nq queries per head against a key/value sequence of Nk >= Nq
+ * tokens, e.g. decode (Nq = 1) or a prefill chunk against a K/V cache
+ * ("CUDA FlashAttention: from online softmax to the long-sequence IO limit",
+ * section 7: split-KV / flash-decoding for long K/V and small B*H, GQA/MQA).
+ *
+ *   q, o        [B, H, Nq, D]                                   (as for fa_fwd)
+ *   k, v        [B, H_kv, Nk, D] (H a multiple of H_kv)
+ *   lse         [B, H, Nq] fp32
+ *   causal      query i is the token at position i + Nk - Nq: with causal = 1
+ *               it sees keys j <= i + Nk - Nq (the mask of fa_fwd when Nq = Nk;
+ *               a single query sees every key); requires Nq <= Nk
+ *   num_splits  0: one pass; 1..64: each query block's key range is cut into
+ *               num_splits chunks processed by different CTAs and merged by a
+ *               second kernel, through `workspace` (as for fa_fwd_splitkv,
+ *               at least fa_fwd_kv_workspace_bytes(B, H, Nq, D, num_splits)
+ *               bytes; ignored and may be NULL when num_splits = 0)
+ *
+ * When Nq < 128 and H_kv < H, the query heads that share a K/V head are
+ * processed as one block of (H / H_kv) * Nq rows, so each K/V head is read
+ * once per split.  Other arguments, layouts and errors as for fa_fwd_splitkv.
+ */
+size_t fa_fwd_kv_workspace_bytes(int B, int H, int Nq, int D, int num_splits);
+int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int Nq,
+              int Nk, int D, float scale, int causal, int dtype, int num_splits, void* workspace,
+              size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fa_fwd_fp8 -- the forward pass on 8-bit inputs ("CUDA FlashAttention: from
  * online softmax to the long-sequence IO limit", section 2: FP8 Q/K/V need a
  * per-tensor or per-block scale, and the softmax state stays FP32).
