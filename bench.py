@@ -517,6 +517,84 @@ def run_ours_bwd(args, w):
     return 0
 
 
+# Decode: one new query per head against a long K/V sequence (fa_fwd_kv).
+#   name: (B, H, H_kv, Nq, Nk, D, dtype)
+DECODE_WORKLOADS = {
+    "decode_bf16_b8h32kv8_nk32768d128": (8, 32, 8, 1, 32768, 128, "bf16"),
+    "decode_bf16_b1h32kv8_nk131072d128": (1, 32, 8, 1, 131072, 128, "bf16"),
+}
+
+
+def run_decode(args):
+    """fa_fwd_kv on a decode shape: HBM-bound, reported as the bandwidth of the
+    bytes one call must move (K, V read once, Q read, O and LSE written)."""
+    import torch
+
+    import exact_attention_22_gb300 as fa
+
+    B, H, H_kv, Nq, Nk, D, dtype = DECODE_WORKLOADS[args.decode]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator().manual_seed(args.seed)
+    td = torch.bfloat16 if dtype == "bf16" else torch.float16
+    q = torch.randn(B, H, Nq, D, generator=g).to(td).to(dev)
+    k = torch.randn(B, H_kv, Nk, D, generator=g).to(td).to(dev)
+    v = torch.randn(B, H_kv, Nk, D, generator=g).to(td).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Nq, dtype=torch.float32, device=dev)
+    splits = args.num_splits
+    ws_bytes = fa.fa_fwd_kv_workspace_bytes(B, H, Nq, D, splits) if splits > 0 else 0
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream
+    dt = fa.FA_BF16 if dtype == "bf16" else fa.FA_FP16
+
+    def launch():
+        st = fa.fa_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, H_kv, Nq,
+                          Nk, D, D ** -0.5, 1, dt, splits, ws.data_ptr() if splits > 0 else 0, ws_bytes, handle)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd_kv")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize()
+    if fa.fa_get_device_status(handle) != fa.FA_OK:
+        raise RuntimeError("device status after warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(0) as clocks:
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    nbytes = 2 * B * H_kv * Nk * D * 2 + 2 * B * H * Nq * D * 2 + B * H * Nq * 4
+    gbps = nbytes / (ms * 1e-3) / 1e9
+    _, hbm, peak_kind = measured_peaks()
+    line = {
+        "metric": "decode bytes moved / time (GB/s)", "value": gbps, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": args.decode, "B": B, "H": H, "H_kv": H_kv, "Nq": Nq, "Nk": Nk, "D": D,
+                   "causal": True, "num_splits": splits, "entry": "fa_fwd_kv",
+                   "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                   "ms_p50": statistics.median(step_ms), "ms_min": min(step_ms)},
+        "roofline": {"bound": "hbm", "achieved": gbps, "peak": hbm, "unit": "GB/s", "frac": gbps / hbm,
+                     "traffic": None, "peak_kind": "%s copy bandwidth" % peak_kind},
+        "gpu_launches": args.steps * (2 if splits > 0 else 1),
+        "clocks": clocks.summary(),
+        "kernel_source_sha": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -529,6 +607,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-splits", type=int, default=0,
                     help="time fa_fwd_splitkv with this many K/V chunks per query block (0: fa_fwd)")
+    ap.add_argument("--decode", choices=sorted(DECODE_WORKLOADS), default=None,
+                    help="time fa_fwd_kv on a decode shape (HBM bandwidth); --num-splits selects split-K")
     ap.add_argument("--fp8", action="store_true",
                     help="time fa_fwd_fp8 on the workload's shape with E4M3 inputs (D = 128, N a multiple of 16)")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
@@ -536,6 +616,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.decode:
+        return run_decode(args)
     w = fa_inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
