@@ -254,6 +254,8 @@ def run_ours(args, w):
         (q_h, k_h, v8), scales_h = fa_inputs.make_qkv_fp8(w, seed=args.seed + rank)
         v_h = v8.transpose(2, 3).contiguous()
         scales = [t.to(dev) for t in scales_h]
+    else:
+        q_h, k_h, v_h = fa_inputs.make_qkv(w, seed=args.seed + rank)
     q, k, v = (t.to(dev) for t in (q_h, k_h, v_h))
     o = torch.empty((w.B, w.H, w.N, w.D), dtype=torch.bfloat16, device=dev) if fp8 else torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)

@@ -667,8 +667,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
                 unpack_f32x2(lx2, x0, x1);
                 l = l * alpha + ((lr[0] + lr[1]) + (lr[2] + lr[3])) * fold;
                 ls = ls * alpha + (x0 + x1) * fold;
-                continue;
-            }
+            } else {
             uint64_t lx2 = pack_f32x2(0.f, 0.f);   // sum of the fp32 p (bf16 only)
             uint32_t pk[kTileN / 2];                 // P as packed 16-bit pairs
 #pragma unroll
@@ -713,6 +712,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
                 // log-sum-exp to better than 5e-4.
                 ls = l;
             }
+            }   // 16-bit P
         }
         if (!ok) break;
 
