@@ -68,6 +68,10 @@ def load_library():
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, I, vp, ctypes.c_size_t, vp]
         lib.fa_bwd.restype = I
+        lib.fa_fwd_host_workspace_bytes.argtypes = [I, I, I, I]
+        lib.fa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, I, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_host.restype = I
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -142,6 +146,17 @@ def fa_bwd(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int
                                      int(dtype), workspace, int(workspace_bytes), stream))
 
 
+def fa_fwd_host_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    return int(load_library().fa_fwd_host_workspace_bytes(B, H, N, D))
+
+
+def fa_fwd_host(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, D: int, scale: float,
+                causal: int, dtype: int, workspace: int, workspace_bytes: int, stream: int) -> int:
+    """Direct call of the C entry point (q, k, v, o, lse: page-locked host pointers)."""
+    return int(load_library().fa_fwd_host(q, k, v, o, lse, B, H, N, D, float(scale), int(causal), int(dtype),
+                                          workspace, workspace_bytes, stream))
+
+
 def fa_get_device_status(stream: int) -> int:
     return int(load_library().fa_get_device_status(stream))
 
@@ -190,6 +205,8 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     dt = FA_BF16 if q.dtype == torch.bfloat16 else FA_FP16
+    if num_splits > 0 and H_kv != H:
+        raise ValueError("split-K with grouped K/V heads goes through attention_kv")
     if num_splits > 0:
         need = fa_splitkv_workspace_bytes(B, H, N, D, num_splits)
         if workspace is None:
@@ -201,8 +218,6 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
             raise FaError(st, "fa_fwd_splitkv")
         return out, lse
     if H_kv != H:
-        if num_splits > 0:
-            raise ValueError("split-K with grouped K/V heads is not provided")
         st = fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, H_kv, N, D,
                         scale, int(bool(causal)), dt, handle)
         if st != FA_OK:
@@ -212,6 +227,52 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
                 int(bool(causal)), dt, handle)
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
+    return out, lse
+
+
+def attention_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, workspace=None,
+                   device=None, stream=None, synchronize: bool = True):
+    """O, LSE = attention(Q, K, V) for contiguous fp16/bf16 tensors in PAGE-LOCKED
+    host memory (``tensor.pin_memory()``), through fa_fwd_host: the copies to and
+    from the GPU overlap the kernel.  Outputs are page-locked host tensors,
+    allocated when not given; the device workspace is allocated with torch
+    unless one is given.  With ``synchronize`` the call waits for the results;
+    otherwise they are ready once ``stream`` has been synchronised.
+    """
+    import torch
+
+    for t in (q, k, v):
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError("q, k, v must be page-locked host tensors")
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    if q.dtype not in (torch.float16, torch.bfloat16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype, float16 or bfloat16")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [B, H, N, D]")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=True)
+    need = fa_fwd_host_workspace_bytes(B, H, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    dt = FA_BF16 if q.dtype == torch.bfloat16 else FA_FP16
+    with torch.cuda.device(device):
+        st = fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N, D,
+                         scale, int(bool(causal)), dt, workspace.data_ptr(),
+                         workspace.numel() * workspace.element_size(), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_host")
+    if synchronize:
+        stream.synchronize() if hasattr(stream, "synchronize") else torch.cuda.synchronize(device)
     return out, lse
 
 

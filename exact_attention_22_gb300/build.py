@@ -1,7 +1,7 @@
 """Build the sm_103a CUDA library in-tree: exact_attention_22_gb300/libfa.so.
 
-Two translation units (the forward and the backward pass), compiled in
-parallel with nvcc directly (no cmake, no torch extension machinery) and
+Three translation units (the forward pass, the backward pass and the
+host-buffer entry point), compiled in parallel with nvcc directly (no cmake, no torch extension machinery) and
 linked into one shared library.  One -gencode; nvcc cross-compiles, so this
 works without a GPU.
 """
@@ -14,7 +14,7 @@ import subprocess
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-SRCS = [os.path.join(CSRC, "fa_fwd.cu"), os.path.join(CSRC, "fa_bwd.cu")]
+SRCS = [os.path.join(CSRC, "fa_fwd.cu"), os.path.join(CSRC, "fa_bwd.cu"), os.path.join(CSRC, "fa_host_io.cu")]
 DEPS = SRCS + [os.path.join(CSRC, "sm103_ptx.cuh"), os.path.join(CSRC, "fa_host.cuh"),
                os.path.join(ROOT, "include", "fa.h")]
 LIB = os.path.join(PKG, "libfa.so")

@@ -209,6 +209,46 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v_t, const float* q_sca
                cudaStream_t stream);
 
 /*
+ * fa_fwd_host_workspace_bytes -- bytes of device workspace fa_fwd_host needs:
+ * room for Q, K, V, O (2*B*H*N*D bytes each) and the LSE (4*B*H*N), each
+ * rounded up to 256 bytes.  Returns 0 for invalid sizes (any size < 1, D not
+ * 64 or 128, B*H*N*D >= 2^40).
+ */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int D);
+
+/*
+ * fa_fwd_host -- fa_fwd on tensors held in host memory.  The pages have no
+ * counterpart: this is the library's entry point for callers whose data is
+ * not on the GPU.  It queues, in chunks of whole (b, h) planes, the copy of
+ * Q, K, V to the device, the forward pass of fa_fwd on each chunk as soon as
+ * its inputs have landed, and the copy of O and LSE back, on two copy streams
+ * of the library's own (created once per device) and on `stream`, so that the
+ * copies in both directions overlap the kernel.  Results are bit-identical to
+ * fa_fwd on the same inputs.
+ *
+ *   q, k, v     [B,H,N,D], type `dtype`   (PAGE-LOCKED host memory, read)
+ *   o           [B,H,N,D], type `dtype`   (page-locked host memory, written)
+ *   lse         [B,H,N] fp32               (page-locked host memory, written)
+ *   B, H, N, D, scale, causal, dtype      as for fa_fwd
+ *   workspace   DEVICE memory owned by the caller, 256-byte aligned, at least
+ *               fa_fwd_host_workspace_bytes(B, H, N, D) bytes; overwritten
+ *   stream      CUDA stream: the call is ordered after the work already queued
+ *               on it, and work queued on it afterwards starts after O and LSE
+ *               are back in host memory; returns without waiting
+ *
+ * Returns FA_OK once everything is queued; synchronise `stream` before
+ * reading o or lse.  Pageable or managed host memory, a workspace that is not
+ * device memory or is too small, and outputs that overlap inputs give
+ * FA_ERR_INVALID_ARG before anything is queued; other argument rules and codes
+ * are those of fa_fwd.  Calls from several host threads are serialised while
+ * they queue work; calls that may run at the same time on the GPU must not
+ * share a workspace.
+ */
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                int B, int H, int N, int D, float scale, int causal, int dtype,
+                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fa_bwd_workspace_bytes -- bytes of workspace fa_bwd needs for these sizes:
  * an fp32 dQ accumulator (4*B*H*N*D bytes) and one fp32 value per query row
  * (4*B*H*N), each rounded up to 256 bytes.  Returns 0 for invalid sizes (any

@@ -162,3 +162,39 @@ def _fp8(**kw):
 ])
 def test_fp8_argument_errors_without_gpu(lib, kw, status):
     assert _fp8(**kw) == status
+
+
+def test_host_workspace_size(lib):
+    r256 = lambda x: (x + 255) // 256 * 256
+    t = 2 * 3 * 100 * 128 * 2
+    assert fa.fa_fwd_host_workspace_bytes(2, 3, 100, 128) == 4 * r256(t) + r256(2 * 3 * 100 * 4)
+    for bad in ((0, 1, 1, 64), (1, 0, 1, 64), (1, 1, 0, 64), (1, 1, 1, 96)):
+        assert fa.fa_fwd_host_workspace_bytes(*bad) == 0
+
+
+HOST = dict(q=1 << 20, k=2 << 20, v=3 << 20, o=4 << 20, lse=5 << 20, ws=6 << 20, ws_bytes=1 << 20,
+            B=1, H=2, N=256, D=64, scale=0.125, causal=1, dtype=0)
+
+
+def _host(**kw):
+    a = dict(HOST, **kw)
+    return fa.fa_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"], a["scale"],
+                          a["causal"], a["dtype"], a["ws"], a["ws_bytes"], 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), 2), (dict(B=0), 1), (dict(causal=2), 1), (dict(dtype=3), 1), (dict(scale=math.inf), 1),
+    (dict(q=0), 3), (dict(lse=(5 << 20) + 4), 3), (dict(ws=(6 << 20) + 16), 3),   # workspace needs 256 bytes
+    (dict(ws_bytes=4096), 1),
+    (dict(o=(1 << 20) + 1024), 1),            # o overlaps q
+    (dict(), 1),                              # fake addresses are not page-locked host memory
+])
+def test_host_argument_errors_without_gpu(lib, kw, status):
+    assert _host(**kw) == status
+
+
+def test_host_binding_rejects_device_or_pageable_tensors(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.float16)   # pageable
+    with pytest.raises(ValueError):
+        fa.attention_host(x, x, x)

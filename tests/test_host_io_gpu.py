@@ -1,0 +1,92 @@
+"""fa_fwd_host (tensors in page-locked host memory, copies overlapped with the
+kernel in chunks of (b, h) planes), through the C ABI.
+
+Every plane is computed by the fa_fwd kernel, so the results must equal
+fa_fwd's bit for bit; a small case is also checked against the FP64 oracle
+with the forward's tolerances.  The shapes cover one chunk, several chunks,
+chunk boundaries that must be moved to keep the LSE rows 16-byte aligned (odd
+and even N), and both dtypes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_22_gb300 as fa
+import fa_inputs
+from oracle import fa_ref
+
+pytestmark = pytest.mark.gpu
+
+
+def _pinned(w, seed):
+    return [t.pin_memory() for t in fa_inputs.make_qkv(w, seed=seed)]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,dtype", [
+    (1, 2, 256, 64, False, "fp16"),      # one chunk
+    (2, 3, 333, 128, True, "bf16"),      # one chunk, odd N
+    (1, 16, 2049, 128, True, "fp16"),    # two chunks, chunk size rounded up to 8 planes for N odd
+    (2, 16, 4096, 64, True, "fp16"),     # six chunks
+    (1, 6, 8190, 128, False, "bf16"),    # N = 2 mod 4: chunks of an even number of planes
+])
+def test_equals_device_path(B, H, N, D, causal, dtype):
+    w = fa_inputs.Workload("host", B, H, N, D, causal, dtype)
+    q, k, v = _pinned(w, seed=N + H)
+    o, lse = fa.attention_host(q, k, v, causal=causal, scale=w.scale)
+    assert fa.fa_get_device_status(0) == fa.FA_OK
+    od, ld = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert not o.is_cuda and o.is_pinned()
+    assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
+
+
+def test_against_oracle():
+    w = fa_inputs.WORKLOADS["tiny_fp16_b1h2n256d64"].with_(causal=True)
+    q, k, v = _pinned(w, seed=0)
+    o, lse = fa.attention_host(q, k, v, causal=True, scale=w.scale)
+    o_ref, lse_ref = fa_ref.naive(fa_inputs.bits(q), fa_inputs.bits(k), fa_inputs.bits(v), w.scale, True,
+                                  enc=fa_inputs.enc(w))
+    assert float(np.abs(o.float().numpy() - o_ref).max()) <= 2e-3
+    assert float(np.abs(lse.numpy() - lse_ref).max()) <= 1e-3
+
+
+def test_stream_order_and_workspace_reuse():
+    """Two calls queued back to back on one side stream with one workspace:
+    the second call's copies wait for the first call's, and the stream is
+    ordered after the copies back."""
+    w = fa_inputs.Workload("host2", 1, 16, 1024, 128, True, "fp16")
+    a = _pinned(w, seed=1)
+    b = _pinned(w, seed=2)
+    ws = torch.empty(fa.fa_fwd_host_workspace_bytes(w.B, w.H, w.N, w.D), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    oa, la = fa.attention_host(*a, causal=True, workspace=ws, stream=s, synchronize=False)
+    ob, lb = fa.attention_host(*b, causal=True, workspace=ws, stream=s, synchronize=False)
+    s.synchronize()
+    assert fa.fa_get_device_status(0) == fa.FA_OK
+    for (q, k, v), o, lse in ((a, oa, la), (b, ob, lb)):
+        od, ld = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=True)
+        torch.cuda.synchronize()
+        assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
+
+
+def test_argument_errors_queue_nothing():
+    w = fa_inputs.Workload("host3", 1, 2, 256, 64, False, "fp16")
+    q, k, v = _pinned(w, seed=3)
+    o = torch.full(q.shape, 7.0, dtype=q.dtype).pin_memory()
+    lse = torch.full((1, 2, 256), 7.0).pin_memory()
+    need = fa.fa_fwd_host_workspace_bytes(1, 2, 256, 64)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    pageable = torch.zeros(q.shape, dtype=q.dtype)
+    host_ws = torch.empty(need, dtype=torch.uint8).pin_memory()
+    call = lambda qq, oo, wsp, wsb, D=64: fa.fa_fwd_host(qq.data_ptr(), k.data_ptr(), v.data_ptr(), oo.data_ptr(),
+                                                        lse.data_ptr(), 1, 2, 256, D, w.scale, 0, fa.FA_FP16,
+                                                        wsp, wsb, 0)
+    assert call(pageable, o, ws.data_ptr(), need) == 1            # input not page-locked
+    assert call(q, pageable, ws.data_ptr(), need) == 1            # output not page-locked
+    assert call(q, o, host_ws.data_ptr(), need) == 1              # workspace not device memory
+    assert call(q, o, ws.data_ptr(), need - 256) == 1             # workspace too small
+    assert call(q, o, ws.data_ptr() + 16, need - 256) == 3        # workspace not 256-byte aligned
+    assert call(q, o, ws.data_ptr(), need, D=96) == 2
+    torch.cuda.synchronize()
+    assert (o == 7).all() and (lse == 7).all()
+    assert fa.fa_get_device_status(0) == fa.FA_OK
