@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kMaxChunks = 8;
 constexpr size_t kMinChunkBytes = size_t(8) << 20;   // below this a chunk's copy is launch-bound
+constexpr long long kMinChunkTiles = 128;
 
 // Per-device copy streams and events, created on first use and kept for the
 // life of the process (like a library handle).
@@ -139,10 +140,15 @@ extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o,
     const int st0 = io_state(dev, &io);
     if (st0 != FA_OK) return st0;
 
-    // Chunks of whole (b, h) planes, at most kMaxChunks, none much under 8 MiB.
+    // Chunks of whole (b, h) planes: at most kMaxChunks, none much under 8 MiB
+    // of inputs, and each with at least kMinChunkTiles work tiles of 256 query
+    // rows, so that a chunk's kernel still fills most of the GPU (measured on
+    // GB300: fewer, fuller chunks win once a chunk's kernel outlasts its copy).
     const long long planes = static_cast<long long>(B) * H;
     const size_t plane_bytes = L.tensor / static_cast<size_t>(planes);
     long long n_chunks = static_cast<long long>((3 * L.tensor) / kMinChunkBytes);
+    const long long by_tiles = planes * ((N + 255) / 256) / kMinChunkTiles;
+    if (n_chunks > by_tiles) n_chunks = by_tiles;
     n_chunks = n_chunks < 1 ? 1 : (n_chunks > kMaxChunks ? kMaxChunks : n_chunks);
     if (n_chunks > planes) n_chunks = planes;
     // Chunk starts keep the LSE rows 16-byte aligned: per * N a multiple of 4.

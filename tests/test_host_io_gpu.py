@@ -25,9 +25,10 @@ def _pinned(w, seed):
 @pytest.mark.parametrize("B,H,N,D,causal,dtype", [
     (1, 2, 256, 64, False, "fp16"),      # one chunk
     (2, 3, 333, 128, True, "bf16"),      # one chunk, odd N
-    (1, 16, 2049, 128, True, "fp16"),    # two chunks, chunk size rounded up to 8 planes for N odd
-    (2, 16, 4096, 64, True, "fp16"),     # six chunks
-    (1, 6, 8190, 128, False, "bf16"),    # N = 2 mod 4: chunks of an even number of planes
+    (1, 32, 4097, 64, True, "fp16"),     # four chunks of 8 planes (N odd: a multiple of 4 planes)
+    (2, 16, 4096, 64, True, "fp16"),     # four chunks
+    (1, 24, 8190, 64, False, "bf16"),    # N = 2 mod 4: six chunks of an even number of planes
+    (1, 32, 8192, 128, True, "fp16"),    # the bench workload: eight chunks
 ])
 def test_equals_device_path(B, H, N, D, causal, dtype):
     w = fa_inputs.Workload("host", B, H, N, D, causal, dtype)
