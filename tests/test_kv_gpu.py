@@ -63,6 +63,22 @@ def test_prefill_chunk_against_cache(shape, splits):
     _check(o, lse, q, k, v, True, D ** -0.5, "fp16", "%s splits=%d" % (shape, splits))
 
 
+@pytest.mark.parametrize("splits", [1, 2, 3, 5])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 16, 4, 1, 5000, 128), (2, 4, 4, 128, 3000, 64), (1, 8, 8, 100, 2500, 128)])
+def test_split_chunks_of_short_query_planes(shape, causal, splits):
+    """Planes of at most 128 query rows (one Q tile) split into 1-5 chunks of
+    K/V tiles, including chunks of odd length and the diagonal tiles of the
+    end-aligned causal mask."""
+    B, H, H_kv, Nq, Nk, D = shape
+    dtype = "bf16" if Nq == 1 else "fp16"
+    q, k, v = _inputs(B, H, H_kv, Nq, Nk, D, dtype, seed=Nk + splits)
+    o, lse = fa.attention_kv(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=D ** -0.5, num_splits=splits)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status(0) == fa.FA_OK
+    _check(o, lse, q, k, v, causal, D ** -0.5, dtype, "%s causal=%d splits=%d" % (shape, causal, splits))
+
+
 def test_long_decode_64_splits():
     q, k, v = _inputs(4, 32, 8, 1, 32768, 128, "bf16", seed=3)
     o, lse = fa.attention_kv(q.cuda(), k.cuda(), v.cuda(), causal=True, num_splits=64)
