@@ -513,12 +513,14 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 }
 
 // dQ warpgroup.  Per step it loads the step's dQ from TMEM, frees TMEM, then
-// adds scale * dQ into the fp32 accumulator with red.global.add.  The L2
-// reduction rate, not the instruction count, bounds this: measured on GB300,
-// reductions that cover whole 128-byte lines per warp instruction beat 16-byte
-// vector reductions scattered over 32 rows.  So:
-//   D = 128: TMEM holds dQ^T (lane = head-dim index d, column = query); one
-//            warp instruction adds 32 consecutive d of one query row;
+// adds scale * dQ into the fp32 accumulator with red.global.add.  Measured on
+// GB300, each SM's rate of writes into L2 bounds this (plain stores are hardly
+// faster than reductions, and fewer CTAs reducing does not speed up the
+// others), and whole 128-byte lines per warp instruction beat 16-byte pieces
+// scattered over 32 rows.  So:
+//   D = 128: TMEM holds dQ^T (lane = head-dim index d, column = query); a
+//            4 x 4 transpose among four lanes turns that into 16-byte
+//            reductions, four whole lines (four queries) per warp instruction;
 //   D = 64:  TMEM holds dQ (lane = query row, 64 columns); each thread adds its
 //            row with 16-byte vector reductions (the transposed form would
 //            need M = 128 for 64 head-dim rows and leave half the lanes idle).
@@ -552,14 +554,38 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
             const int q0 = (w.i0 + s) * kTile;
             const float sc = p.scale;
             if constexpr (D == 128) {
+                // This thread holds dQ^T for d = 32 quarter + lane and the tile's 128
+                // queries.  Lanes 4m .. 4m+3 transpose each 4 x 4 block (d x query) with
+                // two butterfly exchanges, after which lane 4m + i holds d = 32 quarter
+                // + 4m .. 4m+3 of one query and adds them with one 16-byte reduction: a
+                // warp instruction then covers four whole 128-byte lines, not one.
                 const int nq = p.N - q0 < kTile ? p.N - q0 : kTile;
-                float* base = p.dq_acc + (static_cast<size_t>(w.bh) * p.N + q0) * D + r;
+                const int i = lane & 3;
+                const bool b0 = (i & 1) != 0, b1 = (i & 2) != 0;
+                float* base = p.dq_acc + (static_cast<size_t>(w.bh) * p.N + q0 + i) * D + 32 * quarter + 4 * (lane >> 2);
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
+                for (int part = 0; part < 4; ++part) {
 #pragma unroll
-                    for (int part = 0; part < 4; ++part)
-                        if (c + 32 * part < nq)
-                            atomicAdd(base + static_cast<size_t>(c + 32 * part) * D, __uint_as_float(v[part][c]) * sc);
+                    for (int c0 = 0; c0 < 32; c0 += 4) {
+                        const float a0 = __uint_as_float(v[part][c0]), a1 = __uint_as_float(v[part][c0 + 1]);
+                        const float a2 = __uint_as_float(v[part][c0 + 2]), a3 = __uint_as_float(v[part][c0 + 3]);
+                        // lane bit 1: keep the query pair (2 b1, 2 b1 + 1), swap the other
+                        const float k0 = b1 ? a2 : a0, k1 = b1 ? a3 : a1;
+                        const float r0 = __shfl_xor_sync(0xffffffffu, b1 ? a0 : a2, 2);
+                        const float r1 = __shfl_xor_sync(0xffffffffu, b1 ? a1 : a3, 2);
+                        // rows (d) i and i^2 of queries i and i^1
+                        const float mii = b0 ? k1 : k0, mij = b0 ? k0 : k1;
+                        const float m2i = b0 ? r1 : r0, m2j = b0 ? r0 : r1;
+                        // lane bit 0: hand query i^1 to lane i^1, get rows i^1 and i^3 of query i
+                        const float t1 = __shfl_xor_sync(0xffffffffu, mij, 1);
+                        const float t3 = __shfl_xor_sync(0xffffffffu, m2j, 1);
+                        // rows i, i^1, i^2, i^3 of query i, put in the order 0 .. 3
+                        const float w0 = b0 ? t1 : mii, w1 = b0 ? mii : t1, w2 = b0 ? t3 : m2i, w3 = b0 ? m2i : t3;
+                        const float o0 = b1 ? w2 : w0, o1 = b1 ? w3 : w1, o2 = b1 ? w0 : w2, o3 = b1 ? w1 : w3;
+                        const int qc = 32 * part + c0;
+                        if (qc + i < nq)
+                            red_add_v4(base + static_cast<size_t>(qc) * D, o0 * sc, o1 * sc, o2 * sc, o3 * sc);
+                    }
                 }
             } else {
                 if (q0 + r < p.N) {
