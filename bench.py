@@ -177,9 +177,10 @@ def _oracle_inputs(w, seed):
     return _INPUT_CACHE[key]
 
 
-def cpu_oracle_sample(w, seconds=12.0, seed=0):
+def cpu_oracle_sample(w, seconds=12.0, seed=0, nthreads=0):
     """Time the FP64 oracle on a bounded, fixed-order sample of the workload's
-    rows.  Returns (TFLOP/s, rows, seconds, threads, flops)."""
+    rows (all host cores, or ``nthreads``).  Returns (TFLOP/s, rows, seconds,
+    threads, flops)."""
     import numpy as np
 
     from oracle import fa_ref
@@ -189,14 +190,14 @@ def cpu_oracle_sample(w, seconds=12.0, seed=0):
     BH, N = w.B * w.H, w.N
     order_bh = rng.integers(0, BH, 1 << 20)
     order_row = rng.integers(0, N, 1 << 20)
-    threads = fa_ref.max_threads()
+    threads = nthreads if nthreads > 0 else fa_ref.max_threads()
     chunk = max(threads * 4, 64)
     done, flops, t_total = 0, 0.0, 0.0
     while (done == 0 or t_total < seconds) and done + chunk <= len(order_row):
         bh = order_bh[done:done + chunk]
         rows = order_row[done:done + chunk]
         t0 = time.perf_counter()
-        fa_ref.naive_rows(qb, kb, vb, w.scale, w.causal, bh, rows, enc=fa_inputs.enc(w))
+        fa_ref.naive_rows(qb, kb, vb, w.scale, w.causal, bh, rows, enc=fa_inputs.enc(w), nthreads=threads)
         t_total += time.perf_counter() - t0
         vis = (rows + 1) if w.causal else np.full(len(rows), N)
         flops += float(np.sum(4.0 * vis * w.D))
@@ -403,10 +404,13 @@ def run_ours(args, w):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         tf, rows, secs, threads, _ = cpu_oracle_sample(w, seconds=args.cpu_seconds)
+        tf1, rows1, secs1, _, _ = cpu_oracle_sample(w, seconds=min(3.0, args.cpu_seconds), nthreads=1)
         line["cpu_baseline"] = {
             "value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": "%d query rows drawn at random from the workload's %d rows, naive FP64 oracle, %.1f s"
-                      % (rows, w.B * w.H * w.N, secs)}
+                      % (rows, w.B * w.H * w.N, secs),
+            "one_thread": {"value": tf1, "unit": "TFLOP/s", "sample": "the first %d rows of the same sample, "
+                           "%.1f s" % (rows1, secs1)}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
