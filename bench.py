@@ -482,18 +482,21 @@ def run_ours_bwd(args, w):
     if status != fa.FA_OK:
         raise fa.FaError(status, "timed region")
 
-    # End to end: H2D of Q, K, V, O, dO, LSE; the call; D2H of dQ, dK, dV.
+    # End to end through fa_bwd_host, the library's entry point for host-resident
+    # tensors: H2D of Q, K, V, O, dO, LSE, the pass, D2H of dQ, dK, dV, in
+    # chunks of heads with the copies overlapping the kernels.
     pins = [t.pin_memory() for t in (q_h, k_h, v_h, o.cpu(), do_h, lse.cpu())]
     devs = [q, k, v, o, do, lse]
     outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
     e2e_steps = max(3, min(args.steps, 30))
+    hws_bytes = fa.fa_bwd_host_workspace_bytes(w.B, w.H, w.N, w.D)
+    hws = torch.empty(hws_bytes, dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        for d_, h_ in zip(devs, pins):
-            d_.copy_(h_, non_blocking=True)
-        launch()
-        for h_, d_ in zip(outs_h, (dq, dk, dv)):
-            h_.copy_(d_, non_blocking=True)
+        st = fa.fa_bwd_host(*(t.data_ptr() for t in pins[:6]), *(t.data_ptr() for t in outs_h), w.B, w.H, w.N, w.D,
+                            w.scale, int(w.causal), dt, hws.data_ptr(), hws_bytes, handle)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_bwd_host")
 
     for _ in range(2):
         e2e_step()
@@ -507,6 +510,14 @@ def run_ours_bwd(args, w):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    status = fa.fa_get_device_status(handle)
+    if status != fa.FA_OK:
+        raise fa.FaError(status, "end-to-end steps")
+    # dK, dV as the device path gave them; dQ up to the order of its fp32 additions
+    if not (torch.equal(outs_h[1], dk.cpu()) and torch.equal(outs_h[2], dv.cpu())):
+        raise RuntimeError("fa_bwd_host dK / dV differ from fa_bwd")
+    if (outs_h[0].float() - dq.cpu().float()).abs().max().item() > 2.0 ** -9 * max(1.0, dq.float().abs().max().item()):
+        raise RuntimeError("fa_bwd_host dQ differs from fa_bwd")
     h2d = sum(t.numel() * t.element_size() for t in devs)
     d2h = sum(t.numel() * t.element_size() for t in (dq, dk, dv))
 
@@ -528,7 +539,7 @@ def run_ours_bwd(args, w):
                      "frac": achieved / peak, "traffic": None,
                      "peak_kind": "%s dense bf16 (burst); fp16/bf16 nominal ratio 1" % peak_kind},
         "e2e": {"value": job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": "fa_bwd_host"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
         "kernel_source_sha": kernel_source_hash(),

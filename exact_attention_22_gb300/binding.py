@@ -72,6 +72,10 @@ def load_library():
         lib.fa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, I, vp, ctypes.c_size_t, vp]
         lib.fa_fwd_host.restype = I
+        lib.fa_bwd_host_workspace_bytes.argtypes = [I, I, I, I]
+        lib.fa_bwd_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, I, vp, ctypes.c_size_t, vp]
+        lib.fa_bwd_host.restype = I
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -155,6 +159,18 @@ def fa_fwd_host(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int
     """Direct call of the C entry point (q, k, v, o, lse: page-locked host pointers)."""
     return int(load_library().fa_fwd_host(q, k, v, o, lse, B, H, N, D, float(scale), int(causal), int(dtype),
                                           workspace, workspace_bytes, stream))
+
+
+def fa_bwd_host_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    return int(load_library().fa_bwd_host_workspace_bytes(B, H, N, D))
+
+
+def fa_bwd_host(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int, B: int, H: int,
+                N: int, D: int, scale: float, causal: int, dtype: int, workspace: int, workspace_bytes: int,
+                stream: int) -> int:
+    """Direct call of the C entry point (all tensors: page-locked host pointers)."""
+    return int(load_library().fa_bwd_host(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, D, float(scale), int(causal),
+                                          int(dtype), workspace, workspace_bytes, stream))
 
 
 def fa_get_device_status(stream: int) -> int:
@@ -274,6 +290,50 @@ def attention_host(q, k, v, causal: bool = False, scale: float | None = None, ou
     if synchronize:
         stream.synchronize() if hasattr(stream, "synchronize") else torch.cuda.synchronize(device)
     return out, lse
+
+
+def attention_backward_host(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = None, dq=None,
+                            dk=None, dv=None, workspace=None, device=None, stream=None, synchronize: bool = True):
+    """dQ, dK, dV for contiguous fp16/bf16 tensors [B,H,N,D] (and the forward's
+    fp32 LSE [B,H,N]) in PAGE-LOCKED host memory, through fa_bwd_host: the
+    copies to and from the GPU overlap the kernels.  Gradients are page-locked
+    host tensors, allocated when not given; the device workspace is allocated
+    with torch unless one is given.  ``synchronize`` as for attention_host.
+    """
+    import torch
+
+    for t in (q, k, v, out, dout, lse):
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError("q, k, v, out, dout and lse must be page-locked host tensors")
+        if not t.is_contiguous():
+            raise ValueError("q, k, v, out, dout and lse must be contiguous")
+    if q.dtype not in (torch.float16, torch.bfloat16) or any(t.dtype != q.dtype for t in (k, v, out, dout)):
+        raise ValueError("q, k, v, out, dout must share one dtype, float16 or bfloat16")
+    if q.dim() != 4 or any(t.shape != q.shape for t in (k, v, out, dout)):
+        raise ValueError("q, k, v, out, dout must all be [B, H, N, D]")
+    B, H, N, D = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
+        raise ValueError("lse must be float32 [B, H, N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    dq, dk, dv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) if g is None else g for g in (dq, dk, dv))
+    need = fa_bwd_host_workspace_bytes(B, H, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    dt = FA_BF16 if q.dtype == torch.bfloat16 else FA_FP16
+    with torch.cuda.device(device):
+        st = fa_bwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D, scale, int(bool(causal)), dt,
+                         workspace.data_ptr(), workspace.numel() * workspace.element_size(), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_host")
+    if synchronize:
+        stream.synchronize() if hasattr(stream, "synchronize") else torch.cuda.synchronize(device)
+    return dq, dk, dv
 
 
 def attention_backward(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None,

@@ -1,12 +1,12 @@
-// fa_host_io.cu -- the forward pass on host-resident tensors.
+// fa_host_io.cu -- the forward and backward passes on host-resident tensors.
 //
-// Q, K, V live in page-locked host memory and O, LSE are wanted there too.
-// The (b, h) planes are cut into chunks; chunk c's inputs are copied to the
-// device on one stream, its forward pass runs on the caller's stream as soon as
-// they have landed, and its outputs are copied back on a third stream, so the
-// copies in both directions overlap the kernel and each other.  Every plane is
-// computed by the same kernel as fa_fwd, so the results are bit-identical to
-// fa_fwd on the same inputs.
+// The inputs live in page-locked host memory and the outputs are wanted there
+// too.  The (b, h) planes are cut into chunks; chunk c's inputs are copied to
+// the device on one stream, its pass (fa_fwd or fa_bwd on the chunk's planes)
+// runs on the caller's stream as soon as they have landed, and its outputs are
+// copied back on a third stream, so the copies in both directions overlap the
+// kernels and each other.  Every plane is computed by the same kernels as the
+// device entry points.
 
 #include <cmath>
 #include <cstddef>
@@ -75,6 +75,49 @@ bool is_pinned_host(const void* ptr) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Planes per chunk: at most kMaxChunks chunks, none much under 8 MiB of inputs,
+// and each with at least kMinChunkTiles work tiles (of `tile_rows` rows of a
+// plane), so that a chunk's kernel still fills most of the GPU (measured on
+// GB300: fewer, fuller chunks win once a chunk's kernel outlasts its copy).
+// Chunk starts keep the LSE rows 16-byte aligned: planes per chunk times N is
+// a multiple of 4.
+long long chunk_planes(long long planes, int N, size_t in_bytes, int tile_rows) {
+    long long n_chunks = static_cast<long long>(in_bytes / kMinChunkBytes);
+    const long long by_tiles = planes * ((N + tile_rows - 1) / tile_rows) / kMinChunkTiles;
+    if (n_chunks > by_tiles) n_chunks = by_tiles;
+    n_chunks = n_chunks < 1 ? 1 : (n_chunks > kMaxChunks ? kMaxChunks : n_chunks);
+    if (n_chunks > planes) n_chunks = planes;
+    const long long g = (N % 4 == 0) ? 1 : (N % 2 == 0 ? 2 : 4);
+    const long long per = (planes + n_chunks - 1) / n_chunks;
+    return (per + g - 1) / g * g;
+}
+
+// Checks shared by the host entry points: every host buffer page-locked, the
+// workspace device memory.
+bool host_buffers_ok(std::initializer_list<const void*> host, const void* workspace) {
+    for (const void* ptr : host)
+        if (!is_pinned_host(ptr)) return false;
+    cudaPointerAttributes wa;
+    if (cudaPointerGetAttributes(&wa, workspace) != cudaSuccess || wa.type != cudaMemoryTypeDevice) {
+        cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
+// Copy streams ordered after the work already queued on `stream`.
+bool pipeline_begin(HostIo* io, cudaStream_t stream) {
+    return cudaEventRecord(io->start, stream) == cudaSuccess &&
+           cudaStreamWaitEvent(io->h2d, io->start, 0) == cudaSuccess &&
+           cudaStreamWaitEvent(io->d2h, io->start, 0) == cudaSuccess;
+}
+
+// `stream` ordered after every copy back, also after an error part-way
+// through (what was queued still completes before later work).
+bool pipeline_end(HostIo* io, cudaStream_t stream) {
+    return cudaEventRecord(io->done, io->d2h) == cudaSuccess && cudaStreamWaitEvent(stream, io->done, 0) == cudaSuccess;
+}
+
 // Device workspace: Q, K, V, O ([B,H,N,D] 16-bit each), then LSE ([B,H,N] fp32).
 struct Layout {
     size_t tensor, lse_bytes, k, v, o, lse, total;
@@ -125,13 +168,7 @@ extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o,
     for (const void* in : ins)
         if (overlaps(o, L.tensor, in, L.tensor) || overlaps(lse, L.lse_bytes, in, L.tensor)) return FA_ERR_INVALID_ARG;
     if (overlaps(o, L.tensor, lse, L.lse_bytes)) return FA_ERR_INVALID_ARG;
-    for (const void* ptr : {q, k, v, static_cast<const void*>(o), static_cast<const void*>(lse)})
-        if (!is_pinned_host(ptr)) return FA_ERR_INVALID_ARG;
-    cudaPointerAttributes wa;
-    if (cudaPointerGetAttributes(&wa, workspace) != cudaSuccess || wa.type != cudaMemoryTypeDevice) {
-        cudaGetLastError();
-        return FA_ERR_INVALID_ARG;
-    }
+    if (!host_buffers_ok({q, k, v, o, lse}, workspace)) return FA_ERR_INVALID_ARG;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
@@ -140,21 +177,10 @@ extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o,
     const int st0 = io_state(dev, &io);
     if (st0 != FA_OK) return st0;
 
-    // Chunks of whole (b, h) planes: at most kMaxChunks, none much under 8 MiB
-    // of inputs, and each with at least kMinChunkTiles work tiles of 256 query
-    // rows, so that a chunk's kernel still fills most of the GPU (measured on
-    // GB300: fewer, fuller chunks win once a chunk's kernel outlasts its copy).
+    // Chunks of whole (b, h) planes; the forward's work tiles are 256 query rows.
     const long long planes = static_cast<long long>(B) * H;
     const size_t plane_bytes = L.tensor / static_cast<size_t>(planes);
-    long long n_chunks = static_cast<long long>((3 * L.tensor) / kMinChunkBytes);
-    const long long by_tiles = planes * ((N + 255) / 256) / kMinChunkTiles;
-    if (n_chunks > by_tiles) n_chunks = by_tiles;
-    n_chunks = n_chunks < 1 ? 1 : (n_chunks > kMaxChunks ? kMaxChunks : n_chunks);
-    if (n_chunks > planes) n_chunks = planes;
-    // Chunk starts keep the LSE rows 16-byte aligned: per * N a multiple of 4.
-    const long long g = (N % 4 == 0) ? 1 : (N % 2 == 0 ? 2 : 4);
-    long long per = (planes + n_chunks - 1) / n_chunks;
-    per = (per + g - 1) / g * g;
+    const long long per = chunk_planes(planes, N, 3 * L.tensor, 256);
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const uint8_t* hq = static_cast<const uint8_t*>(q);
@@ -164,9 +190,7 @@ extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o,
     uint8_t* hl = reinterpret_cast<uint8_t*>(lse);
     const size_t lse_plane = static_cast<size_t>(N) * 4;
 
-    bool ok = cudaEventRecord(io->start, stream) == cudaSuccess &&
-              cudaStreamWaitEvent(io->h2d, io->start, 0) == cudaSuccess &&
-              cudaStreamWaitEvent(io->d2h, io->start, 0) == cudaSuccess;
+    bool ok = pipeline_begin(io, stream);
     int status = ok ? FA_OK : FA_ERR_CUDA;
     for (int c = 0; ok && c * per < planes; ++c) {
         const long long p0 = c * per, np = (planes - p0 < per) ? planes - p0 : per;
@@ -190,9 +214,123 @@ extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o,
              cudaMemcpyAsync(hl + loff, ws + L.lse + loff, llen, cudaMemcpyDeviceToHost, io->d2h) == cudaSuccess;
         if (!ok && status == FA_OK) status = FA_ERR_CUDA;
     }
-    // The caller's stream is ordered after every copy back, also on an error
-    // part-way through (what was queued still completes before later work).
-    if (cudaEventRecord(io->done, io->d2h) != cudaSuccess || cudaStreamWaitEvent(stream, io->done, 0) != cudaSuccess)
-        status = FA_ERR_CUDA;
+    if (!pipeline_end(io, stream)) status = FA_ERR_CUDA;
+    return status;
+}
+
+// ------------------------------------------------------------------ backward
+
+namespace fa103 {
+namespace {
+
+// Device workspace of fa_bwd_host: Q, K, V, O, dO, dQ, dK, dV ([B,H,N,D]
+// 16-bit each), the LSE ([B,H,N] fp32), then fa_bwd's own workspace for one
+// chunk (reused by the chunks in turn: they run one after another on the
+// caller's stream).
+struct BwdLayout {
+    size_t tensor, lse_bytes, stride, lse, bws, bws_bytes, total;
+    long long per;
+};
+
+bool bwd_layout(int B, int H, int N, int D, BwdLayout* L) {
+    if (B < 1 || H < 1 || N < 1 || (D != 64 && D != 128)) return false;
+    const uint64_t planes = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
+    const uint64_t elems = planes * static_cast<uint64_t>(N) * D;
+    if (planes > 0x7fffffffull || elems >= (uint64_t(1) << 40)) return false;
+    L->tensor = static_cast<size_t>(elems) * 2;
+    L->lse_bytes = static_cast<size_t>(elems / D) * 4;
+    L->stride = align256(L->tensor);
+    L->lse = 8 * L->stride;
+    L->per = chunk_planes(static_cast<long long>(planes), N, 5 * L->tensor, 128);
+    L->bws = L->lse + align256(L->lse_bytes);
+    L->bws_bytes = fa_bwd_workspace_bytes(1, static_cast<int>(L->per), N, D);
+    if (L->bws_bytes == 0) return false;
+    L->total = L->bws + L->bws_bytes;
+    return true;
+}
+
+}  // namespace
+}  // namespace fa103
+
+extern "C" size_t fa_bwd_host_workspace_bytes(int B, int H, int N, int D) {
+    BwdLayout L;
+    return bwd_layout(B, H, N, D, &L) ? L.total : 0;
+}
+
+extern "C" int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                           const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale,
+                           int causal, int dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    // The argument rules of fa_bwd, checked here so that nothing is queued on
+    // an error.
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    BwdLayout L;
+    if (!bwd_layout(B, H, N, D, &L)) return FA_ERR_INVALID_ARG;
+    const void* ptrs[10] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+    for (const void* ptr : ptrs)
+        if (ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return FA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_MISALIGNED;
+    if (workspace_bytes < L.total) return FA_ERR_INVALID_ARG;
+    const void* ins[6] = {q, k, v, o, dout, lse};
+    const size_t in_bytes[6] = {L.tensor, L.tensor, L.tensor, L.tensor, L.tensor, L.lse_bytes};
+    const void* outs[3] = {dq, dk, dv};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlaps(outs[a], L.tensor, ins[b], in_bytes[b])) return FA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 3; ++b)
+            if (overlaps(outs[a], L.tensor, outs[b], L.tensor)) return FA_ERR_INVALID_ARG;
+    }
+    if (!host_buffers_ok({q, k, v, o, dout, lse, dq, dk, dv}, workspace)) return FA_ERR_INVALID_ARG;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_io_mutex);
+    HostIo* io = nullptr;
+    const int st0 = io_state(dev, &io);
+    if (st0 != FA_OK) return st0;
+
+    // Chunks of whole (b, h) planes; the backward's work tiles are 128 keys.
+    const long long planes = static_cast<long long>(B) * H;
+    const size_t plane_bytes = L.tensor / static_cast<size_t>(planes);
+    const size_t lse_plane = static_cast<size_t>(N) * 4;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const uint8_t* hin[5] = {static_cast<const uint8_t*>(q), static_cast<const uint8_t*>(k),
+                             static_cast<const uint8_t*>(v), static_cast<const uint8_t*>(o),
+                             static_cast<const uint8_t*>(dout)};
+    uint8_t* hout[3] = {static_cast<uint8_t*>(dq), static_cast<uint8_t*>(dk), static_cast<uint8_t*>(dv)};
+    const uint8_t* hl = reinterpret_cast<const uint8_t*>(lse);
+
+    bool ok = pipeline_begin(io, stream);
+    int status = ok ? FA_OK : FA_ERR_CUDA;
+    for (int c = 0; ok && c * L.per < planes; ++c) {
+        const long long p0 = c * L.per, np = (planes - p0 < L.per) ? planes - p0 : L.per;
+        const size_t off = static_cast<size_t>(p0) * plane_bytes, len = static_cast<size_t>(np) * plane_bytes;
+        const size_t loff = static_cast<size_t>(p0) * lse_plane, llen = static_cast<size_t>(np) * lse_plane;
+        for (int t = 0; ok && t < 5; ++t)
+            ok = cudaMemcpyAsync(ws + t * L.stride + off, hin[t] + off, len, cudaMemcpyHostToDevice, io->h2d) ==
+                 cudaSuccess;
+        ok = ok &&
+             cudaMemcpyAsync(ws + L.lse + loff, hl + loff, llen, cudaMemcpyHostToDevice, io->h2d) == cudaSuccess &&
+             cudaEventRecord(io->in[c], io->h2d) == cudaSuccess &&
+             cudaStreamWaitEvent(stream, io->in[c], 0) == cudaSuccess;
+        if (!ok) {
+            status = FA_ERR_CUDA;
+            break;
+        }
+        status = fa_bwd(ws + off, ws + L.stride + off, ws + 2 * L.stride + off, ws + 3 * L.stride + off,
+                        ws + 4 * L.stride + off, reinterpret_cast<const float*>(ws + L.lse + loff),
+                        ws + 5 * L.stride + off, ws + 6 * L.stride + off, ws + 7 * L.stride + off, 1,
+                        static_cast<int>(np), N, D, scale, causal, dtype, ws + L.bws, L.bws_bytes, stream);
+        ok = status == FA_OK && cudaEventRecord(io->out[c], stream) == cudaSuccess &&
+             cudaStreamWaitEvent(io->d2h, io->out[c], 0) == cudaSuccess;
+        for (int t = 0; ok && t < 3; ++t)
+            ok = cudaMemcpyAsync(hout[t] + off, ws + (5 + t) * L.stride + off, len, cudaMemcpyDeviceToHost,
+                                 io->d2h) == cudaSuccess;
+        if (!ok && status == FA_OK) status = FA_ERR_CUDA;
+    }
+    if (!pipeline_end(io, stream)) status = FA_ERR_CUDA;
     return status;
 }

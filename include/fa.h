@@ -292,6 +292,39 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fa_bwd_host_workspace_bytes -- bytes of device workspace fa_bwd_host needs:
+ * room for Q, K, V, O, dO, dQ, dK, dV (2*B*H*N*D bytes each) and the LSE
+ * (4*B*H*N), each rounded up to 256 bytes, plus fa_bwd's workspace for one
+ * chunk of (b, h) planes.  Returns 0 for invalid sizes (any size < 1, D not
+ * 64 or 128, B*H*N*D >= 2^40).
+ */
+size_t fa_bwd_host_workspace_bytes(int B, int H, int N, int D);
+
+/*
+ * fa_bwd_host -- fa_bwd on tensors held in host memory, the backward
+ * counterpart of fa_fwd_host (no counterpart on the pages).  In chunks of
+ * whole (b, h) planes it queues the copy of Q, K, V, O, dO and LSE to the
+ * device, fa_bwd on the chunk once they have landed, and the copy of dQ, dK
+ * and dV back, on the library's two copy streams and on `stream`, so that the
+ * copies overlap the kernels.  dK and dV are bit-identical to fa_bwd's; dQ is
+ * accumulated with fp32 atomics, as in fa_bwd, and may differ in its last bits.
+ *
+ *   q, k, v, o, dout    [B,H,N,D], type `dtype`   (PAGE-LOCKED host memory, read)
+ *   lse                 [B,H,N] fp32              (page-locked host memory, read)
+ *   dq, dk, dv          [B,H,N,D], type `dtype`   (page-locked host memory, written)
+ *   B, H, N, D, scale, causal, dtype              as for fa_bwd
+ *   workspace           DEVICE memory owned by the caller, 256-byte aligned, at
+ *                       least fa_bwd_host_workspace_bytes(B, H, N, D) bytes;
+ *                       overwritten
+ *   stream              as for fa_fwd_host
+ *
+ * Errors and ordering as for fa_fwd_host.
+ */
+int fa_bwd_host(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale, int causal, int dtype,
+                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fa_get_device_status -- synchronise `stream`, then report whether any
  * kernel of this library on the current device gave up on a bounded wait
  * since the last call (FA_ERR_TIMEOUT; the outputs of that launch are

@@ -198,3 +198,34 @@ def test_host_binding_rejects_device_or_pageable_tensors(lib):
     x = torch.zeros(1, 1, 8, 64, dtype=torch.float16)   # pageable
     with pytest.raises(ValueError):
         fa.attention_host(x, x, x)
+
+
+def test_bwd_host_workspace_size(lib):
+    r256 = lambda x: (x + 255) // 256 * 256
+    t = 2 * 3 * 100 * 64 * 2
+    # one chunk here (small problem): fa_bwd's workspace for all 6 planes
+    assert fa.fa_bwd_host_workspace_bytes(2, 3, 100, 64) == 8 * r256(t) + r256(600 * 4) + \
+        fa.fa_bwd_workspace_bytes(1, 6, 100, 64)
+    for bad in ((0, 1, 1, 64), (1, 0, 1, 64), (1, 1, 0, 64), (1, 1, 1, 96)):
+        assert fa.fa_bwd_host_workspace_bytes(*bad) == 0
+
+
+BWDH = dict(q=1 << 20, k=2 << 20, v=3 << 20, o=4 << 20, dout=5 << 20, lse=6 << 20, dq=7 << 20, dk=8 << 20,
+            dv=9 << 20, ws=10 << 20, ws_bytes=4 << 20, B=1, H=2, N=256, D=64, scale=0.125, causal=1, dtype=0)
+
+
+def _bwd_host(**kw):
+    a = dict(BWDH, **kw)
+    return fa.fa_bwd_host(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"], a["B"],
+                          a["H"], a["N"], a["D"], a["scale"], a["causal"], a["dtype"], a["ws"], a["ws_bytes"], 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(D=96), 2), (dict(N=0), 1), (dict(causal=2), 1), (dict(scale=0.0), 1),
+    (dict(dq=0), 3), (dict(ws=(10 << 20) + 16), 3), (dict(ws_bytes=1024), 1),
+    (dict(dq=(1 << 20) + 1024), 1),           # dq overlaps q
+    (dict(dk=(9 << 20) - 4096), 1),           # dk overlaps dv
+    (dict(), 1),                              # fake addresses are not page-locked host memory
+])
+def test_bwd_host_argument_errors_without_gpu(lib, kw, status):
+    assert _bwd_host(**kw) == status

@@ -1,11 +1,12 @@
-"""fa_fwd_host (tensors in page-locked host memory, copies overlapped with the
-kernel in chunks of (b, h) planes), through the C ABI.
+"""fa_fwd_host and fa_bwd_host (tensors in page-locked host memory, copies
+overlapped with the kernels in chunks of (b, h) planes), through the C ABI.
 
-Every plane is computed by the fa_fwd kernel, so the results must equal
-fa_fwd's bit for bit; a small case is also checked against the FP64 oracle
-with the forward's tolerances.  The shapes cover one chunk, several chunks,
-chunk boundaries that must be moved to keep the LSE rows 16-byte aligned (odd
-and even N), and both dtypes.
+Every plane is computed by the device kernels, so the forward results must
+equal fa_fwd's bit for bit, and dK, dV fa_bwd's (dQ is summed with fp32
+atomics in both, so only the order of its additions differs); small cases are
+also checked against the FP64 oracle with the device paths' tolerances.  The
+shapes cover one chunk, several chunks, chunk boundaries that must be moved to
+keep the LSE rows 16-byte aligned (odd and even N), and both dtypes.
 """
 import numpy as np
 import pytest
@@ -90,4 +91,61 @@ def test_argument_errors_queue_nothing():
     assert call(q, o, ws.data_ptr(), need, D=96) == 2
     torch.cuda.synchronize()
     assert (o == 7).all() and (lse == 7).all()
+    assert fa.fa_get_device_status(0) == fa.FA_OK
+
+
+# ------------------------------------------------------------------ fa_bwd_host
+
+def _bwd_pinned(w, seed):
+    q, k, v = fa_inputs.make_qkv(w, seed=seed)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(seed + 1)).to(q.dtype)
+    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, scale=w.scale)
+    return [t.pin_memory() for t in (q, k, v, o.cpu(), do, lse.cpu())]
+
+
+@pytest.mark.parametrize("B,H,N,D,causal,dtype", [
+    (1, 2, 256, 64, True, "fp16"),       # one chunk
+    (2, 3, 333, 128, False, "bf16"),     # one chunk, odd N
+    (1, 16, 4097, 64, True, "fp16"),     # four chunks of 4 planes (N odd)
+    (1, 32, 8192, 128, True, "fp16"),    # the bench workload: eight chunks
+])
+def test_backward_equals_device_path(B, H, N, D, causal, dtype):
+    w = fa_inputs.Workload("bwdhost", B, H, N, D, causal, dtype)
+    q, k, v, o, do, lse = _bwd_pinned(w, seed=N + D)
+    dq, dk, dv = fa.attention_backward_host(q, k, v, o, lse, do, causal=causal, scale=w.scale)
+    assert fa.fa_get_device_status(0) == fa.FA_OK
+    assert not dq.is_cuda and dq.is_pinned()
+    rq, rk, rv = fa.attention_backward(*(t.cuda() for t in (q, k, v, o, lse, do)), causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(dk, rk.cpu()) and torch.equal(dv, rv.cpu())
+    # dQ: fp32 atomics in both, so only the order of the additions differs
+    tol = 2.0 ** -9 * max(1.0, rq.float().abs().max().item())
+    assert (dq.float() - rq.cpu().float()).abs().max().item() <= tol
+
+
+def test_backward_against_oracle():
+    w = fa_inputs.WORKLOADS["tiny_fp16_b1h2n256d64"].with_(causal=True)
+    q, k, v, o, do, lse = _bwd_pinned(w, seed=5)
+    dq, dk, dv = fa.attention_backward_host(q, k, v, o, lse, do, causal=True, scale=w.scale)
+    refs = fa_ref.backward(*(fa_inputs.bits(t) for t in (q, k, v, do)), w.scale, True, enc=fa_inputs.enc(w))
+    for got, ref in zip((dq, dk, dv), refs):
+        assert float(np.abs(got.float().numpy() - ref).max()) <= 2.0 ** -9 * max(1.0, float(np.abs(ref).max()))
+
+
+def test_backward_argument_errors_queue_nothing():
+    w = fa_inputs.Workload("bwdhost3", 1, 2, 256, 64, False, "fp16")
+    q, k, v, o, do, lse = _bwd_pinned(w, seed=9)
+    dq, dk, dv = (torch.full(q.shape, 7.0, dtype=q.dtype).pin_memory() for _ in range(3))
+    need = fa.fa_bwd_host_workspace_bytes(1, 2, 256, 64)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    pageable = torch.zeros(q.shape, dtype=q.dtype)
+    call = lambda dout, g, wsb: fa.fa_bwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                               dout.data_ptr(), lse.data_ptr(), g.data_ptr(), dk.data_ptr(),
+                                               dv.data_ptr(), 1, 2, 256, 64, w.scale, 0, fa.FA_FP16, ws.data_ptr(),
+                                               wsb, 0)
+    assert call(pageable, dq, need) == 1          # dO not page-locked
+    assert call(do, pageable, need) == 1          # dQ not page-locked
+    assert call(do, dq, need - 256) == 1          # workspace too small
+    torch.cuda.synchronize()
+    assert all((g == 7).all() for g in (dq, dk, dv))
     assert fa.fa_get_device_status(0) == fa.FA_OK
