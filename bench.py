@@ -620,6 +620,25 @@ def run_decode(args):
         torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     ms = sum(step_ms) / len(step_ms)
+    if fa.fa_get_device_status(handle) != fa.FA_OK:
+        raise RuntimeError("device status after the timed region")
+    # End to end: a decode step's new queries come from the host and its outputs
+    # go back; the K/V cache stays resident on the device, as it does in serving.
+    q_h = q.cpu().pin_memory()
+    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        q.copy_(q_h, non_blocking=True)
+        launch()
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
     nbytes = 2 * B * H_kv * Nk * D * 2 + 2 * B * H * Nq * D * 2 + B * H * Nq * 4
     gbps = nbytes / (ms * 1e-3) / 1e9
     _, hbm, peak_kind = measured_peaks()
@@ -633,6 +652,10 @@ def run_decode(args):
                    "ms_p50": statistics.median(step_ms), "ms_p95": p95(step_ms), "ms_min": min(step_ms)},
         "roofline": {"bound": "hbm", "achieved": gbps, "peak": hbm, "unit": "GB/s", "frac": gbps / hbm,
                      "traffic": None, "peak_kind": "%s copy bandwidth" % peak_kind},
+        "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": q.numel() * q.element_size(),
+                "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size(),
+                "api": "copy of Q, fa_fwd_kv, copy of O and LSE; the K/V cache resident on the device"},
         "gpu_launches": args.steps * (2 if splits > 0 else 1),
         "clocks": clocks.summary(),
         "kernel_source_sha": kernel_source_hash(),

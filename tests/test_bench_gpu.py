@@ -11,7 +11,7 @@ pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
-        "vs_baseline", "dtype", "data", "config", "roofline", "gpu_launches", "clocks"}
+        "vs_baseline", "dtype", "data", "config", "roofline", "gpu_launches", "clocks", "e2e"}
 
 
 def _run(*args):
@@ -22,7 +22,8 @@ def _run(*args):
     assert len(lines) == 1, out.stdout
     d = json.loads(lines[0])
     assert KEYS <= set(d), sorted(KEYS - set(d))
-    assert d["value"] > 0 and d["roofline"]["frac"] > 0
+    assert d["value"] > 0 and d["roofline"]["frac"] > 0 and d["e2e"]["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     return d
 
 
