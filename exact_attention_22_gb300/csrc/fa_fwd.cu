@@ -72,10 +72,12 @@ constexpr int kThreads = 128 * (2 + kNumQ);   // producer/MMA WG, softmax WGs, c
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;   // 1 s per wait
 constexpr float kLazyRescale = 8.0f;          // log2 units: rescale only when the max grows > 2^8
 // FP8 path: P is stored as E4M3 (largest finite 448).  A lag of the reference
-// max of up to 2 log2 units and a range shift of 2^6 keep P <= 2^8, while
-// probabilities down to 2^-12 stay normal numbers of the format.
-constexpr float kLazyRescaleFp8 = 2.0f;
-constexpr float kFp8Shift = 6.0f;
+// max of up to 3 log2 units and a range shift of 2^5 keep P <= 2^8, while
+// probabilities down to 2^-11 stay normal numbers of the format.  (A lag of 2
+// with a shift of 2^6 rescaled O more often and ran 4-7% slower.)
+constexpr float kLazyRescaleFp8 = 3.0f;
+constexpr float kFp8Shift = 5.0f;
+constexpr float kFp8ShiftScale = 32.0f;   // 2^kFp8Shift
 constexpr uint32_t kTmemCols = 512;
 
 template <int D, bool FP8 = false>
@@ -549,7 +551,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
         // FP8: S is the product of the E4M3 values; the scores are S times the
         // Q and K block scales, folded into the exponent's coefficient.  P V adds
         // E4M3 V^T bytes: each tile's V block scale, relative to the head's largest
-        // (v_ref), and a range shift of 2^6 are folded into P (see the pack below).
+        // (v_ref), and a range shift of 2^kFp8Shift are folded into P (see the pack below).
         float c_q = scale_log2, v_ref = 1.f;
         if constexpr (FP8) {
             c_q = scale_log2 * __ldg(p.q_scale + static_cast<size_t>(w.bh) * p.n_blocks + (w.q0 + kTileM * t) / kTileM);
@@ -578,7 +580,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
                 const float vs = __ldg(p.v_scale + kb);
                 c_s = c_q * __ldg(p.k_scale + kb);
                 shift = kFp8Shift + log2f(vs / v_ref);
-                fold = v_ref / (vs * 64.f);
+                fold = v_ref / (vs * kFp8ShiftScale);
             }
             // Causal: the row's query is the token at position qpos of the key
             // sequence (qi + Nk - Nq; with stacked heads, its position within its
@@ -641,7 +643,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             const uint64_t c2 = pack_f32x2(cf, cf);
             const uint64_t nm2 = pack_f32x2(shift - msub, shift - msub);
             if constexpr (FP8) {
-                // P'' = 2^(s c - m_ref + shift) = p * 2^6 * vs / v_ref, four per E4M3 word
+                // P'' = 2^(s c - m_ref + shift) = p * 2^kFp8Shift * vs / v_ref, four per E4M3 word
                 uint64_t lx2 = pack_f32x2(0.f, 0.f);   // sum of the unrounded P''
                 uint32_t pk8[kTileN / 4];
 #pragma unroll
@@ -741,8 +743,8 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             tc_fence_before();
             continue;
         }
-        // FP8: O holds sum P'' v8 = 2^6 / v_ref * sum p (vs v8); undo the fold
-        const float inv = l > 0.f ? (FP8 ? v_ref * 0.015625f : 1.f) / l : 0.f;
+        // FP8: O holds sum P'' v8 = 2^kFp8Shift / v_ref * sum p (vs v8); undo the fold
+        const float inv = l > 0.f ? (FP8 ? v_ref / kFp8ShiftScale : 1.f) / l : 0.f;
         uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + (row_ok ? row_g : 0) * D);
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
