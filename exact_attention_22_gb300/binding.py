@@ -61,6 +61,8 @@ def load_library():
         lib.fa_fwd_kv_workspace_bytes.argtypes = [I, I, I, I, I]
         lib.fa_fwd_kv_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, I, F, I, I, I, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_kv_splits_hint.argtypes = [I, I, I, I, I, I, I]
+        lib.fa_fwd_kv_splits_hint.restype = I
         lib.fa_fwd_kv.restype = I
         lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, vp]
         lib.fa_fwd_fp8.restype = I
@@ -130,6 +132,10 @@ def fa_fwd_kv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, H_kv: in
     """Direct call of the queries-against-a-K/V-sequence entry point; returns its status code."""
     return int(load_library().fa_fwd_kv(q, k, v, o, lse, B, H, H_kv, Nq, Nk, D, float(scale), int(causal),
                                         int(dtype), int(num_splits), workspace, int(workspace_bytes), stream))
+
+
+def fa_fwd_kv_splits_hint(B: int, H: int, H_kv: int, Nq: int, Nk: int, D: int, causal: int) -> int:
+    return int(load_library().fa_fwd_kv_splits_hint(B, H, H_kv, Nq, Nk, D, int(causal)))
 
 
 def fa_fwd_fp8(q: int, k: int, v_t: int, q_scale: int, k_scale: int, v_scale: int, o: int, lse: int, B: int, H: int,
@@ -412,11 +418,12 @@ def attention_fp8(q8, k8, v8_t, q_scale, k_scale, v_scale, causal: bool = False,
     return out, lse
 
 
-def attention_kv(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 0, out=None, lse=None,
+def attention_kv(q, k, v, causal: bool = False, scale: float | None = None, num_splits=0, out=None, lse=None,
                  workspace=None, stream=None):
     """O, LSE for q [B,H,Nq,D] against k, v [B,H_kv,Nk,D] (fp16/bf16 CUDA tensors;
     query i is the token at position i + Nk - Nq).  ``num_splits`` > 0 selects
-    split-K with a torch-allocated workspace unless one is given."""
+    split-K with a torch-allocated workspace unless one is given; "auto" takes
+    fa_fwd_kv_splits_hint's choice."""
     import torch
 
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -429,6 +436,11 @@ def attention_kv(q, k, v, causal: bool = False, scale: float | None = None, num_
         raise ValueError("q, k, v must be contiguous")
     B, H, Nq, D = q.shape
     H_kv, Nk = k.shape[1], k.shape[2]
+    if num_splits == "auto":
+        with torch.cuda.device(q.device):
+            num_splits = fa_fwd_kv_splits_hint(B, H, H_kv, Nq, Nk, D, int(bool(causal)))
+        if num_splits < 0:
+            raise FaError(1, "fa_fwd_kv_splits_hint")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     out = torch.empty_like(q) if out is None else out

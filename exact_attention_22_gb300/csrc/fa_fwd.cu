@@ -1164,6 +1164,32 @@ extern "C" int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, f
     return dispatch_merge(p, D, dtype, stream);
 }
 
+// Split count for fa_fwd_kv: enough work tiles to cover the SMs once (twice
+// for causal blocks of several query blocks, whose work per block differs),
+// each chunk at least 4 K/V tiles, at most kMaxSplits; 0 when the unsplit grid
+// already covers the SMs.
+extern "C" int fa_fwd_kv_splits_hint(int B, int H, int H_kv, int Nq, int Nk, int D, int causal) {
+    if (B < 1 || H < 1 || H_kv < 1 || Nq < 1 || Nk < 1 || H % H_kv != 0 || (D != 64 && D != 128)) return -1;
+    if (causal != 0 && causal != 1) return -1;
+    if (causal && Nq > Nk) return -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return -1;
+    const bool pack = H_kv < H && Nq < kTileM;
+    const long long planes = static_cast<long long>(B) * (pack ? H_kv : H);
+    const long long rows = pack ? static_cast<long long>(H / H_kv) * Nq : Nq;
+    const long long qblocks = (rows + kRowsPerTile - 1) / kRowsPerTile;
+    const long long base = planes * qblocks;
+    const long long target = static_cast<long long>(sms) * ((causal && qblocks > 1) ? 2 : 1);
+    if (base >= target) return 0;
+    long long s = target / base;
+    const long long kv_tiles = (static_cast<long long>(Nk) + kTileN - 1) / kTileN;
+    if (s > kv_tiles / 4) s = kv_tiles / 4;
+    if (s > kMaxSplits) s = kMaxSplits;
+    return s >= 2 ? static_cast<int>(s) : 0;
+}
+
 // ------------------------------------------------------------------ FP8 forward
 namespace fa103 {
 

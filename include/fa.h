@@ -173,6 +173,17 @@ size_t fa_noalloc_scratch_bytes(void);
  * once per split.  Other arguments, layouts and errors as for fa_fwd_splitkv.
  */
 size_t fa_fwd_kv_workspace_bytes(int B, int H, int Nq, int D, int num_splits);
+
+/*
+ * fa_fwd_kv_splits_hint -- a num_splits for fa_fwd_kv on the current device:
+ * 0 when the unsplit grid of work tiles already covers the SMs, else enough
+ * chunks per query block to cover them once (twice for causal problems of
+ * several 256-row query blocks, whose blocks differ in work), each chunk at
+ * least 4 key/value tiles, at most 64.  A host-side rule of thumb, not a
+ * measurement.  Returns -1 for invalid sizes (as for fa_fwd_kv) or if the
+ * device cannot be queried.
+ */
+int fa_fwd_kv_splits_hint(int B, int H, int H_kv, int Nq, int Nk, int D, int causal);
 int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int Nq,
               int Nk, int D, float scale, int causal, int dtype, int num_splits, void* workspace,
               size_t workspace_bytes, cudaStream_t stream);

@@ -229,3 +229,9 @@ def _bwd_host(**kw):
 ])
 def test_bwd_host_argument_errors_without_gpu(lib, kw, status):
     assert _bwd_host(**kw) == status
+
+
+@pytest.mark.parametrize("args", [(0, 32, 8, 1, 4096, 128, 1), (1, 32, 6, 1, 4096, 128, 1), (1, 32, 8, 1, 4096, 96, 1),
+                                  (1, 32, 8, 8, 4, 128, 1), (1, 32, 8, 1, 4096, 128, 2)])
+def test_kv_splits_hint_rejects_invalid_sizes(lib, args):
+    assert fa.fa_fwd_kv_splits_hint(*args) == -1

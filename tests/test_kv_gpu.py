@@ -79,6 +79,21 @@ def test_split_chunks_of_short_query_planes(shape, causal, splits):
     _check(o, lse, q, k, v, causal, D ** -0.5, dtype, "%s causal=%d splits=%d" % (shape, causal, splits))
 
 
+def test_splits_hint_and_auto_mode():
+    """The hint splits decode shapes whose unsplit grid leaves SMs idle and leaves
+    large problems unsplit; num_splits="auto" gives the oracle's result."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert fa.fa_fwd_kv_splits_hint(8, 32, 8, 1, 32768, 128, 1) == (sms // 64 if sms // 64 >= 2 else 0)
+    assert fa.fa_fwd_kv_splits_hint(1, 32, 8, 1, 131072, 128, 1) == min(64, sms // 8)
+    assert fa.fa_fwd_kv_splits_hint(1, 32, 32, 4096, 4096, 128, 1) == 0      # 512 work tiles
+    assert fa.fa_fwd_kv_splits_hint(1, 1, 1, 32768, 32768, 128, 1) >= 2      # one long causal head
+    q, k, v = _inputs(2, 16, 4, 1, 9000, 128, "bf16", seed=77)
+    o, lse = fa.attention_kv(q.cuda(), k.cuda(), v.cuda(), causal=True, num_splits="auto")
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status(0) == fa.FA_OK
+    _check(o, lse, q, k, v, True, 128 ** -0.5, "bf16", "auto splits")
+
+
 def test_long_decode_64_splits():
     q, k, v = _inputs(4, 32, 8, 1, 32768, 128, "bf16", seed=3)
     o, lse = fa.attention_kv(q.cuda(), k.cuda(), v.cuda(), causal=True, num_splits=64)
