@@ -588,7 +588,12 @@ def run_decode(args):
     v = torch.randn(B, H_kv, Nk, D, generator=g).to(td).to(dev)
     o = torch.empty_like(q)
     lse = torch.empty(B, H, Nq, dtype=torch.float32, device=dev)
-    splits = args.num_splits
+    if args.num_splits_auto:
+        splits = fa.fa_fwd_kv_splits_hint(B, H, H_kv, Nq, Nk, D, 1)
+        if splits < 0:
+            raise RuntimeError("fa_fwd_kv_splits_hint failed")
+    else:
+        splits = args.num_splits
     ws_bytes = fa.fa_fwd_kv_workspace_bytes(B, H, Nq, D, splits) if splits > 0 else 0
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -674,8 +679,9 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--num-splits", type=int, default=0,
-                    help="time fa_fwd_splitkv with this many K/V chunks per query block (0: fa_fwd)")
+    ap.add_argument("--num-splits", default="0",
+                    help="time fa_fwd_splitkv with this many K/V chunks per query block (0: fa_fwd); with "
+                         "--decode, 'auto' takes fa_fwd_kv_splits_hint's count")
     ap.add_argument("--decode", choices=sorted(DECODE_WORKLOADS), default=None,
                     help="time fa_fwd_kv on a decode shape (HBM bandwidth); --num-splits selects split-K")
     ap.add_argument("--fp8", action="store_true",
@@ -683,6 +689,10 @@ def main(argv=None):
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward pass (default, the headline) or the backward pass")
     args = ap.parse_args(argv)
+    args.num_splits_auto = args.num_splits == "auto"
+    if args.num_splits_auto and args.decode is None:
+        ap.error("--num-splits auto applies to --decode")
+    args.num_splits = 0 if args.num_splits_auto else int(args.num_splits)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.decode:

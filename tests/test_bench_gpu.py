@@ -33,6 +33,7 @@ def test_default_forward_line():
 
 
 @pytest.mark.parametrize("extra", [["--pass", "bwd", "--no-cpu-baseline"], ["--fp8", "--no-cpu-baseline"],
-                                   ["--decode", "decode_bf16_b8h32kv8_nk32768d128", "--num-splits", "2"]])
+                                   ["--decode", "decode_bf16_b8h32kv8_nk32768d128", "--num-splits", "2"],
+                                   ["--decode", "decode_bf16_b1h32kv8_nk131072d128", "--num-splits", "auto"]])
 def test_other_modes(extra):
     _run(*extra)
