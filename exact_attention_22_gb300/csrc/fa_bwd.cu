@@ -521,15 +521,17 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 //   D = 128: TMEM holds dQ^T (lane = head-dim index d, column = query); a
 //            4 x 4 transpose among four lanes turns that into 16-byte
 //            reductions, four whole lines (four queries) per warp instruction;
-//   D = 64:  TMEM holds dQ (lane = query row, 64 columns); each thread adds its
-//            row with 16-byte vector reductions (the transposed form would
+//   D = 64:  TMEM holds dQ (lane = query row, 64 columns); groups of eight
+//            lanes transpose their 8 x 8 blocks of 16-byte pieces, so that a
+//            16-byte reduction instruction covers four whole lines (four
+//            rows) instead of pieces of 32 rows (the transposed dQ^T would
 //            need M = 128 for 64 head-dim rows and leave half the lanes idle).
 template <int D, bool CAUSAL>
 __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
     using C = Cfg<D>;
     volatile int* abort_flag = &st.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
-    const int r = 32 * quarter + lane;   // TMEM lane: d (D = 128) or query row (D = 64)
+    // TMEM lane 32 quarter + lane: head-dim index d (D = 128) or query row (D = 64)
     const uint32_t tA = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + C::kTmA;
     constexpr int kCols = D == 128 ? kTile : D;   // TMEM columns of the step's dQ
     int g = 0;
@@ -588,14 +590,41 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
                     }
                 }
             } else {
-                if (q0 + r < p.N) {
-                    float* row = p.dq_acc + (static_cast<size_t>(w.bh) * p.N + q0 + r) * D;
+                // This thread holds the query row q0 + r (64 columns).  Per 32-column
+                // half, eight lanes (eight rows) transpose their 8 x 8 block of 16-byte
+                // pieces with three butterfly exchanges, after which lane 8g + b holds
+                // piece b of rows 8g .. 8g+7: a warp instruction then adds four whole
+                // 128-byte lines (one piece-row of four groups) instead of 32 pieces.
+                const int b = lane & 7, g = lane >> 3;
+                const int row0 = q0 + 32 * quarter + 8 * g;   // first row of this lane's group
+                float* gbase = p.dq_acc + (static_cast<size_t>(w.bh) * p.N + row0) * D + 4 * b;
 #pragma unroll
-                    for (int c = 0; c < kCols / 32; ++c)
+                for (int c = 0; c < kCols / 32; ++c) {
+                    float a[8][4];
 #pragma unroll
-                        for (int e = 0; e < 32; e += 4)
-                            red_add_v4(row + 32 * c + e, __uint_as_float(v[c][e]) * sc, __uint_as_float(v[c][e + 1]) * sc,
-                                       __uint_as_float(v[c][e + 2]) * sc, __uint_as_float(v[c][e + 3]) * sc);
+                    for (int e = 0; e < 8; ++e)
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) a[e][x] = __uint_as_float(v[c][4 * e + x]) * sc;
+#pragma unroll
+                    for (int d = 4; d >= 1; d >>= 1) {
+                        const bool hi_lane = (lane & d) != 0;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            if (e & d) continue;
+#pragma unroll
+                            for (int x = 0; x < 4; ++x) {
+                                // send the piece whose bit d differs from this lane's
+                                const float snd = hi_lane ? a[e][x] : a[e | d][x];
+                                const float rcv = __shfl_xor_sync(0xffffffffu, snd, d);
+                                if (hi_lane) a[e][x] = rcv;
+                                else a[e | d][x] = rcv;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (row0 + i < p.N)
+                            red_add_v4(gbase + static_cast<size_t>(i) * D + 32 * c, a[i][0], a[i][1], a[i][2], a[i][3]);
                 }
             }
         }
