@@ -326,12 +326,22 @@ def run_ours(args, w):
     qp, kp, vp = (t.pin_memory() for t in (q_h, k_h, v_h))
     op = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     lp = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    host_api = not fp8 and splits == 0
+    host_api = splits == 0
     if host_api:
-        hws_bytes = fa.fa_fwd_host_workspace_bytes(w.B, w.H, w.N, w.D)
+        hws_bytes = (fa.fa_fwd_fp8_host_workspace_bytes if fp8 else fa.fa_fwd_host_workspace_bytes)(w.B, w.H, w.N,
+                                                                                                    w.D)
         hws = torch.empty(hws_bytes, dtype=torch.uint8, device=dev)
+        if fp8:
+            scp = [t.pin_memory() for t in scales_h]
 
     def e2e_step():
+        if host_api and fp8:
+            st = fa.fa_fwd_fp8_host(qp.data_ptr(), kp.data_ptr(), vp.data_ptr(), scp[0].data_ptr(), scp[1].data_ptr(),
+                                    scp[2].data_ptr(), op.data_ptr(), lp.data_ptr(), w.B, w.H, w.N, w.D, w.scale,
+                                    int(w.causal), hws.data_ptr(), hws_bytes, handle)
+            if st != fa.FA_OK:
+                raise fa.FaError(st, "fa_fwd_fp8_host")
+            return
         if host_api:
             st = fa.fa_fwd_host(qp.data_ptr(), kp.data_ptr(), vp.data_ptr(), op.data_ptr(), lp.data_ptr(), w.B, w.H,
                                 w.N, w.D, w.scale, int(w.causal), dt, hws.data_ptr(), hws_bytes, handle)
@@ -361,8 +371,10 @@ def run_ours(args, w):
             raise fa.FaError(status, "end-to-end steps")
         # the host-buffer path computes what the device path computed
         if not (torch.equal(op, o.cpu()) and torch.equal(lp, lse.cpu())):
-            raise RuntimeError("fa_fwd_host results differ from fa_fwd")
+            raise RuntimeError("host-buffer entry results differ from the device entry's")
     h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    if fp8:
+        h2d += sum(t.numel() * t.element_size() for t in scales_h)   # the block scales travel too
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
 
     total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], device=dev)
@@ -396,8 +408,8 @@ def run_ours(args, w):
                      "peak_kind": peak_note,
                      "effective_GBps": w.io_bytes / (ms_per_step * 1e-3) / 1e9},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "api": "fa_fwd_host" if host_api else "copies + %s + copies in order" %
-                ("fa_fwd_fp8" if fp8 else "fa_fwd_splitkv")},
+                "ms_per_step": e2e_ms, "api": ("fa_fwd_fp8_host" if fp8 else "fa_fwd_host") if host_api else
+                "copies + fa_fwd_splitkv + copies in order"},
         "gpu_launches": launches,
         "clocks": clk,
         "kernel_source_sha": kernel_source_hash(),

@@ -78,6 +78,10 @@ def load_library():
         lib.fa_bwd_host_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_bwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, I, vp, ctypes.c_size_t, vp]
         lib.fa_bwd_host.restype = I
+        lib.fa_fwd_fp8_host_workspace_bytes.argtypes = [I, I, I, I]
+        lib.fa_fwd_fp8_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_fwd_fp8_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, vp, ctypes.c_size_t, vp]
+        lib.fa_fwd_fp8_host.restype = I
         lib.fa_status_string.argtypes = [I]
         lib.fa_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -177,6 +181,18 @@ def fa_bwd_host(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk
     """Direct call of the C entry point (all tensors: page-locked host pointers)."""
     return int(load_library().fa_bwd_host(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, D, float(scale), int(causal),
                                           int(dtype), workspace, workspace_bytes, stream))
+
+
+def fa_fwd_fp8_host_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    return int(load_library().fa_fwd_fp8_host_workspace_bytes(B, H, N, D))
+
+
+def fa_fwd_fp8_host(q: int, k: int, v_t: int, q_scale: int, k_scale: int, v_scale: int, o: int, lse: int, B: int,
+                    H: int, N: int, D: int, scale: float, causal: int, workspace: int, workspace_bytes: int,
+                    stream: int) -> int:
+    """Direct call of the C entry point (all tensors: page-locked host pointers)."""
+    return int(load_library().fa_fwd_fp8_host(q, k, v_t, q_scale, k_scale, v_scale, o, lse, B, H, N, D,
+                                              float(scale), int(causal), workspace, workspace_bytes, stream))
 
 
 def fa_get_device_status(stream: int) -> int:

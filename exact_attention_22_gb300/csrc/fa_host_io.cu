@@ -334,3 +334,128 @@ extern "C" int fa_bwd_host(const void* q, const void* k, const void* v, const vo
     if (!pipeline_end(io, stream)) status = FA_ERR_CUDA;
     return status;
 }
+
+// ------------------------------------------------------------------ FP8 forward
+
+namespace fa103 {
+namespace {
+
+// Device workspace of fa_fwd_fp8_host: Q, K (E4M3 [B,H,N,D]), V^T (E4M3
+// [B,H,D,N]), the three block-scale arrays ([B,H,ceil(N/128)] fp32), O (bf16
+// [B,H,N,D]) and the LSE ([B,H,N] fp32), each rounded up to 256 bytes.
+struct Fp8Layout {
+    size_t elems, sc_bytes, o_bytes, lse_bytes, k, vt, qs, ks, vs, o, lse, total;
+    int n_blocks;
+};
+
+bool fp8_layout(int B, int H, int N, int D, Fp8Layout* L) {
+    if (B < 1 || H < 1 || N < 1 || D != 128 || N % 16 != 0) return false;
+    const uint64_t planes = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
+    const uint64_t elems = planes * static_cast<uint64_t>(N) * D;
+    if (planes > 0x7fffffffull || elems >= (uint64_t(1) << 40)) return false;
+    L->n_blocks = (N + 127) / 128;
+    L->elems = static_cast<size_t>(elems);
+    L->sc_bytes = static_cast<size_t>(planes) * L->n_blocks * 4;
+    L->o_bytes = L->elems * 2;
+    L->lse_bytes = static_cast<size_t>(planes) * N * 4;
+    L->k = align256(L->elems);
+    L->vt = L->k + align256(L->elems);
+    L->qs = L->vt + align256(L->elems);
+    L->ks = L->qs + align256(L->sc_bytes);
+    L->vs = L->ks + align256(L->sc_bytes);
+    L->o = L->vs + align256(L->sc_bytes);
+    L->lse = L->o + align256(L->o_bytes);
+    L->total = L->lse + align256(L->lse_bytes);
+    return true;
+}
+
+}  // namespace
+}  // namespace fa103
+
+extern "C" size_t fa_fwd_fp8_host_workspace_bytes(int B, int H, int N, int D) {
+    Fp8Layout L;
+    return fp8_layout(B, H, N, D, &L) ? L.total : 0;
+}
+
+extern "C" int fa_fwd_fp8_host(const void* q, const void* k, const void* v_t, const float* q_scale,
+                               const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H, int N,
+                               int D, float scale, int causal, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+    // The argument rules of fa_fwd_fp8, checked here so that nothing is queued
+    // on an error.
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+    if (D != 128) return FA_ERR_UNSUPPORTED;
+    if (N % 16 != 0) return FA_ERR_INVALID_ARG;
+    Fp8Layout L;
+    if (!fp8_layout(B, H, N, D, &L)) return FA_ERR_INVALID_ARG;
+    const void* ptrs[9] = {q, k, v_t, q_scale, k_scale, v_scale, o, lse, workspace};
+    for (const void* ptr : ptrs)
+        if (ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return FA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FA_ERR_MISALIGNED;
+    if (workspace_bytes < L.total) return FA_ERR_INVALID_ARG;
+    const void* ins[6] = {q, k, v_t, q_scale, k_scale, v_scale};
+    const size_t ib[6] = {L.elems, L.elems, L.elems, L.sc_bytes, L.sc_bytes, L.sc_bytes};
+    for (int i = 0; i < 6; ++i)
+        if (overlaps(o, L.o_bytes, ins[i], ib[i]) || overlaps(lse, L.lse_bytes, ins[i], ib[i]))
+            return FA_ERR_INVALID_ARG;
+    if (overlaps(o, L.o_bytes, lse, L.lse_bytes)) return FA_ERR_INVALID_ARG;
+    if (!host_buffers_ok({q, k, v_t, q_scale, k_scale, v_scale, o, lse}, workspace)) return FA_ERR_INVALID_ARG;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_io_mutex);
+    HostIo* io = nullptr;
+    const int st0 = io_state(dev, &io);
+    if (st0 != FA_OK) return st0;
+
+    // Chunks of whole planes; chunk starts also keep the block scales 16-byte
+    // aligned (planes per chunk times the blocks per plane a multiple of 4).
+    const long long planes = static_cast<long long>(B) * H;
+    long long per = chunk_planes(planes, N, 3 * L.elems, 256);
+    const long long g = (L.n_blocks % 4 == 0) ? 1 : (L.n_blocks % 2 == 0 ? 2 : 4);
+    per = (per + g - 1) / g * g;
+    const size_t plane_in = L.elems / static_cast<size_t>(planes), plane_sc = static_cast<size_t>(L.n_blocks) * 4;
+    const size_t plane_o = plane_in * 2, plane_l = static_cast<size_t>(N) * 4;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const uint8_t* hin[3] = {static_cast<const uint8_t*>(q), static_cast<const uint8_t*>(k),
+                             static_cast<const uint8_t*>(v_t)};
+    const size_t din[3] = {0, L.k, L.vt};
+    const uint8_t* hsc[3] = {reinterpret_cast<const uint8_t*>(q_scale), reinterpret_cast<const uint8_t*>(k_scale),
+                             reinterpret_cast<const uint8_t*>(v_scale)};
+    const size_t dsc[3] = {L.qs, L.ks, L.vs};
+
+    bool ok = pipeline_begin(io, stream);
+    int status = ok ? FA_OK : FA_ERR_CUDA;
+    for (int c = 0; ok && c * per < planes; ++c) {
+        const long long p0 = c * per, np = (planes - p0 < per) ? planes - p0 : per;
+        const size_t p0s = static_cast<size_t>(p0), nps = static_cast<size_t>(np);
+        for (int t = 0; ok && t < 3; ++t)
+            ok = cudaMemcpyAsync(ws + din[t] + p0s * plane_in, hin[t] + p0s * plane_in, nps * plane_in,
+                                 cudaMemcpyHostToDevice, io->h2d) == cudaSuccess &&
+                 cudaMemcpyAsync(ws + dsc[t] + p0s * plane_sc, hsc[t] + p0s * plane_sc, nps * plane_sc,
+                                 cudaMemcpyHostToDevice, io->h2d) == cudaSuccess;
+        ok = ok && cudaEventRecord(io->in[c], io->h2d) == cudaSuccess &&
+             cudaStreamWaitEvent(stream, io->in[c], 0) == cudaSuccess;
+        if (!ok) {
+            status = FA_ERR_CUDA;
+            break;
+        }
+        status = fa_fwd_fp8(ws + p0s * plane_in, ws + L.k + p0s * plane_in, ws + L.vt + p0s * plane_in,
+                            reinterpret_cast<const float*>(ws + L.qs + p0s * plane_sc),
+                            reinterpret_cast<const float*>(ws + L.ks + p0s * plane_sc),
+                            reinterpret_cast<const float*>(ws + L.vs + p0s * plane_sc), ws + L.o + p0s * plane_o,
+                            reinterpret_cast<float*>(ws + L.lse + p0s * plane_l), 1, static_cast<int>(np), N, D,
+                            scale, causal, stream);
+        ok = status == FA_OK && cudaEventRecord(io->out[c], stream) == cudaSuccess &&
+             cudaStreamWaitEvent(io->d2h, io->out[c], 0) == cudaSuccess &&
+             cudaMemcpyAsync(static_cast<uint8_t*>(o) + p0s * plane_o, ws + L.o + p0s * plane_o, nps * plane_o,
+                             cudaMemcpyDeviceToHost, io->d2h) == cudaSuccess &&
+             cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + p0s * plane_l, ws + L.lse + p0s * plane_l,
+                             nps * plane_l, cudaMemcpyDeviceToHost, io->d2h) == cudaSuccess;
+        if (!ok && status == FA_OK) status = FA_ERR_CUDA;
+    }
+    if (!pipeline_end(io, stream)) status = FA_ERR_CUDA;
+    return status;
+}

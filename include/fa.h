@@ -303,6 +303,27 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fa_fwd_fp8_host_workspace_bytes -- bytes of device workspace fa_fwd_fp8_host
+ * needs: room for Q, K, V^T (B*H*N*D bytes each), the three scale arrays
+ * (4*B*H*ceil(N/128) bytes each), O (2*B*H*N*D) and the LSE (4*B*H*N), each
+ * rounded up to 256 bytes.  Returns 0 for invalid sizes (any size < 1, D not
+ * 128, N not a multiple of 16).
+ */
+size_t fa_fwd_fp8_host_workspace_bytes(int B, int H, int N, int D);
+
+/*
+ * fa_fwd_fp8_host -- fa_fwd_fp8 on tensors held in host memory, the FP8
+ * counterpart of fa_fwd_host: all of q, k, v_t, the three scale arrays, o and
+ * lse are PAGE-LOCKED host memory (layouts as for fa_fwd_fp8); the workspace
+ * is device memory, 256-byte aligned, at least
+ * fa_fwd_fp8_host_workspace_bytes(B, H, N, D) bytes.  Results are
+ * bit-identical to fa_fwd_fp8's.  Errors and ordering as for fa_fwd_host.
+ */
+int fa_fwd_fp8_host(const void* q, const void* k, const void* v_t, const float* q_scale, const float* k_scale,
+                    const float* v_scale, void* o, float* lse, int B, int H, int N, int D, float scale, int causal,
+                    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fa_bwd_host_workspace_bytes -- bytes of device workspace fa_bwd_host needs:
  * room for Q, K, V, O, dO, dQ, dK, dV (2*B*H*N*D bytes each) and the LSE
  * (4*B*H*N), each rounded up to 256 bytes, plus fa_bwd's workspace for one

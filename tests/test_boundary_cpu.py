@@ -235,3 +235,20 @@ def test_bwd_host_argument_errors_without_gpu(lib, kw, status):
                                   (1, 32, 8, 8, 4, 128, 1), (1, 32, 8, 1, 4096, 128, 2)])
 def test_kv_splits_hint_rejects_invalid_sizes(lib, args):
     assert fa.fa_fwd_kv_splits_hint(*args) == -1
+
+
+def test_fp8_host_workspace_size_and_errors(lib):
+    r256 = lambda x: (x + 255) // 256 * 256
+    e = 2 * 3 * 256 * 128
+    sc = 2 * 3 * 2 * 4
+    assert fa.fa_fwd_fp8_host_workspace_bytes(2, 3, 256, 128) == 3 * r256(e) + 3 * r256(sc) + r256(2 * e) + \
+        r256(2 * 3 * 256 * 4)
+    for bad in ((0, 1, 16, 128), (1, 1, 100, 128), (1, 1, 256, 64)):
+        assert fa.fa_fwd_fp8_host_workspace_bytes(*bad) == 0
+    a = [1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20, 6 << 20, 7 << 20, 8 << 20]
+    call = lambda N=256, D=128, ws=10 << 20, wsb=64 << 20: fa.fa_fwd_fp8_host(*a, 1, 2, N, D, 0.09, 1, ws, wsb, 0)
+    assert call(D=64) == 2
+    assert call(N=100) == 1
+    assert call(ws=(10 << 20) + 16) == 3
+    assert call(wsb=1024) == 1
+    assert call() == 1          # fake addresses are not page-locked host memory

@@ -149,3 +149,26 @@ def test_backward_argument_errors_queue_nothing():
     torch.cuda.synchronize()
     assert all((g == 7).all() for g in (dq, dk, dv))
     assert fa.fa_get_device_status(0) == fa.FA_OK
+
+
+# ------------------------------------------------------------------ fa_fwd_fp8_host
+
+@pytest.mark.parametrize("B,H,N,causal", [(1, 2, 256, False), (2, 3, 400, True), (1, 32, 4096, True)])
+def test_fp8_equals_device_path(B, H, N, causal):
+    w = fa_inputs.Workload("fp8host", B, H, N, 128, causal, "bf16")
+    (q8, k8, v8), scs = fa_inputs.make_qkv_fp8(w, seed=N)
+    vt = v8.transpose(2, 3).contiguous()
+    hq, hk, hv = (t.pin_memory() for t in (q8, k8, vt))
+    hs = [t.pin_memory() for t in scs]
+    o = torch.empty((B, H, N, 128), dtype=torch.bfloat16).pin_memory()
+    lse = torch.empty((B, H, N)).pin_memory()
+    nb = fa.fa_fwd_fp8_host_workspace_bytes(B, H, N, 128)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    st = fa.fa_fwd_fp8_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), *(t.data_ptr() for t in hs), o.data_ptr(),
+                            lse.data_ptr(), B, H, N, 128, w.scale, int(causal), ws.data_ptr(), nb, 0)
+    assert st == fa.FA_OK
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status(0) == fa.FA_OK
+    od, ld = fa.attention_fp8(q8.cuda(), k8.cuda(), vt.cuda(), *(t.cuda() for t in scs), causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o, od.cpu()) and torch.equal(lse, ld.cpu())
