@@ -4,11 +4,10 @@
 // The inputs live in page-locked host memory and the outputs are wanted there
 // too.  The (b, h) planes are cut into chunks; chunk c's inputs are copied to
 // the device on one stream, its pass (fa_fwd, fa_fwd_fp8 or fa_bwd on the
-// chunk's planes)
-// runs on the caller's stream as soon as they have landed, and its outputs are
-// copied back on a third stream, so the copies in both directions overlap the
-// kernels and each other.  Every plane is computed by the same kernels as the
-// device entry points.
+// chunk's planes) runs on the caller's stream as soon as they have landed, and
+// its outputs are copied back on a third stream, so the copies in both
+// directions overlap the kernels and each other.  Every plane is computed by the
+// same kernels as the device entry points.
 
 #include <cmath>
 #include <cstddef>
