@@ -6,7 +6,7 @@ CPU or PyTorch fallback: if the library is missing, importing the binding
 raises.
 """
 from .binding import (FA_BF16, FA_FP16, FA_OK, FaError, STATUS_NAMES, attention, attention_backward,  # noqa: F401
-                      attention_backward_host, attention_fp8, attention_host, attention_kv, fa_bwd, fa_bwd_host,
+                      attention_backward_host, attention_fp8, attention_host, attention_kv, fa_bwd, fa_bwd_gqa, fa_bwd_host,
                       fa_bwd_host_workspace_bytes, fa_bwd_workspace_bytes, fa_fwd, fa_fwd_fp8, fa_fwd_fp8_host,
                       fa_fwd_fp8_host_workspace_bytes,
                       fa_fwd_gqa, fa_fwd_host, fa_fwd_host_workspace_bytes, fa_fwd_kv, fa_fwd_kv_splits_hint,

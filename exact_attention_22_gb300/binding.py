@@ -70,6 +70,8 @@ def load_library():
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, I, I, I, I, F, I, I, vp, ctypes.c_size_t, vp]
         lib.fa_bwd.restype = I
+        lib.fa_bwd_gqa.argtypes = [vp] * 9 + [I, I, I, I, I, F, I, I, vp, ctypes.c_size_t, vp]
+        lib.fa_bwd_gqa.restype = I
         lib.fa_fwd_host_workspace_bytes.argtypes = [I, I, I, I]
         lib.fa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, I, vp, ctypes.c_size_t, vp]
@@ -193,6 +195,14 @@ def fa_fwd_fp8_host(q: int, k: int, v_t: int, q_scale: int, k_scale: int, v_scal
     """Direct call of the C entry point (all tensors: page-locked host pointers)."""
     return int(load_library().fa_fwd_fp8_host(q, k, v_t, q_scale, k_scale, v_scale, o, lse, B, H, N, D,
                                               float(scale), int(causal), workspace, workspace_bytes, stream))
+
+
+def fa_bwd_gqa(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int, B: int, H: int,
+               H_kv: int, N: int, D: int, scale: float, causal: int, dtype: int, workspace: int,
+               workspace_bytes: int, stream: int) -> int:
+    """Direct call of the C entry point; returns its status code."""
+    return int(load_library().fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, D, float(scale),
+                                         int(causal), int(dtype), workspace, workspace_bytes, stream))
 
 
 def fa_get_device_status(stream: int) -> int:
@@ -360,10 +370,12 @@ def attention_backward_host(q, k, v, out, lse, dout, causal: bool = False, scale
 
 def attention_backward(q, k, v, out, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None,
                        dv=None, workspace=None, stream=None):
-    """dQ, dK, dV of attention for contiguous fp16/bf16 CUDA tensors [B,H,N,D]:
-    ``out`` and ``lse`` are the forward pass's outputs, ``dout`` the upstream
-    gradient.  Gradients (and the workspace) are allocated with torch when not
-    given.  Raises FaError on a non-OK status.  Asynchronous on ``stream``."""
+    """dQ, dK, dV of attention for contiguous fp16/bf16 CUDA tensors: q, out,
+    dout [B,H,N,D] and k, v [B,H_kv,N,D] (H_kv = H, or a divisor of H for
+    grouped K/V heads); ``out`` and ``lse`` are the forward pass's outputs,
+    ``dout`` the upstream gradient.  Gradients (and the workspace) are
+    allocated with torch when not given.  Raises FaError on a non-OK status.
+    Asynchronous on ``stream``."""
     import torch
 
     ts = (q, k, v, out, dout)
@@ -371,9 +383,11 @@ def attention_backward(q, k, v, out, lse, dout, causal: bool = False, scale: flo
         raise ValueError("all tensors must be CUDA tensors")
     if q.dtype not in (torch.float16, torch.bfloat16) or any(t.dtype != q.dtype for t in ts):
         raise ValueError("q, k, v, out, dout must share one dtype, float16 or bfloat16")
-    if q.dim() != 4 or any(t.shape != q.shape for t in ts):
-        raise ValueError("q, k, v, out, dout must all be [B, H, N, D]")
+    if q.dim() != 4 or out.shape != q.shape or dout.shape != q.shape or k.dim() != 4 or v.shape != k.shape or \
+            k.shape[0] != q.shape[0] or k.shape[2:] != q.shape[2:] or q.shape[1] % k.shape[1] != 0:
+        raise ValueError("q, out, dout must be [B, H, N, D] and k, v [B, H_kv, N, D] with H_kv dividing H")
     B, H, N, D = q.shape
+    H_kv = k.shape[1]
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N):
         raise ValueError("lse must be float32 [B, H, N]")
     if not all(t.is_contiguous() for t in ts + (lse,)):
@@ -381,8 +395,8 @@ def attention_backward(q, k, v, out, lse, dout, causal: bool = False, scale: flo
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(q) if dk is None else dk
-    dv = torch.empty_like(q) if dv is None else dv
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(k) if dv is None else dv
     need = fa_bwd_workspace_bytes(B, H, N, D)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -390,11 +404,11 @@ def attention_backward(q, k, v, out, lse, dout, causal: bool = False, scale: flo
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     dt = FA_BF16 if q.dtype == torch.bfloat16 else FA_FP16
-    st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(), lse.data_ptr(),
-                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D, scale, int(bool(causal)), dt,
-                workspace.data_ptr(), workspace.numel() * workspace.element_size(), handle)
+    st = fa_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, H_kv, N, D, scale, int(bool(causal)), dt,
+                    workspace.data_ptr(), workspace.numel() * workspace.element_size(), handle)
     if st != FA_OK:
-        raise FaError(st, "fa_bwd")
+        raise FaError(st, "fa_bwd_gqa")
     return dq, dk, dv
 
 

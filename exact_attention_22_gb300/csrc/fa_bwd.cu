@@ -107,26 +107,41 @@ struct Params {
     const float* lse;     // [BH, N] natural log
     const float* delta;   // [BH, N]
     int N;
-    int BH;
+    int BH;               // query planes B * H
+    int BHkv;             // K/V planes B * H_kv
+    int H, H_kv;          // query heads and K/V heads per batch entry
+    int G;                // H / H_kv: query heads per K/V head
     int T;                // ceil(N / 128)
-    int n_tiles;          // BH * T
+    int n_tiles;          // BHkv * T
     float scale;
     float scale_log2;     // scale * log2(e)
 };
 
-// Work tile: K/V tile j of head bh, visited by Q tiles i0 .. i0 + n - 1.
+// Work tile: K/V tile j of K/V plane kvbh.  Its steps visit Q tiles
+// i0 .. T - 1 of each of the G query heads that share the K/V head, head by
+// head (n_per steps each, n in all), so dK and dV sum over the group in TMEM.
 struct Work {
-    int bh, j, i0, n;
+    int kvbh, j, i0, n_per, n, qbh0;
 };
 
 template <bool CAUSAL>
 __device__ __forceinline__ Work make_work(const Params& p, int idx) {
     Work w;
-    w.j = idx / p.BH;   // j-major: under the causal mask tile j has T - j steps, heaviest first
-    w.bh = idx - w.j * p.BH;
+    w.j = idx / p.BHkv;   // j-major: under the causal mask tile j has T - j steps, heaviest first
+    w.kvbh = idx - w.j * p.BHkv;
     w.i0 = CAUSAL ? w.j : 0;
-    w.n = p.T - w.i0;
+    w.n_per = p.T - w.i0;
+    w.n = p.G * w.n_per;
+    w.qbh0 = (w.kvbh / p.H_kv) * p.H + (w.kvbh % p.H_kv) * p.G;
     return w;
+}
+// Q tile and query plane of the next step: Q tiles i0 .. T - 1 of one query
+// head, then of the next (counters kept by each role, so no division per step).
+__device__ __forceinline__ void step_next(const Work& w, int T, int& qi, int& qbh) {
+    if (++qi == T) {
+        qi = w.i0;
+        ++qbh;
+    }
 }
 
 // Work tile of this CTA's k-th turn: snake order over the CTAs.
@@ -202,14 +217,15 @@ __device__ void run_load(State& st, uint8_t* smem, const CUtensorMap* tm_q, cons
         }
         mbar_arrive_expect_tx(&st.kv_full, 2 * C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b) {
-            tma_load_3d_hint(smem + C::kOffK + b * C::kBoxBytes, tm_k, &st.kv_full, 64 * b, w.j * kTile, w.bh,
+            tma_load_3d_hint(smem + C::kOffK + b * C::kBoxBytes, tm_k, &st.kv_full, 64 * b, w.j * kTile, w.kvbh,
                              pol_once);
-            tma_load_3d_hint(smem + C::kOffV + b * C::kBoxBytes, tm_v, &st.kv_full, 64 * b, w.j * kTile, w.bh,
+            tma_load_3d_hint(smem + C::kOffV + b * C::kBoxBytes, tm_v, &st.kv_full, 64 * b, w.j * kTile, w.kvbh,
                              pol_once);
         }
         ++kv_loads;
-        for (int s = 0; s < w.n && ok; ++s, ++g) {
-            const int i = w.i0 + s, slot = g & 1;
+        int i = w.i0, qbh = w.qbh0;
+        for (int s = 0; s < w.n && ok; ++s, ++g, step_next(w, p.T, i, qbh)) {
+            const int slot = g & 1;
             const uint32_t ph = ((g >> 1) & 1) ^ 1;
             if (!wait_bar(&st.q_empty[slot], ph, abort_flag)) {
                 ok = false;
@@ -218,7 +234,7 @@ __device__ void run_load(State& st, uint8_t* smem, const CUtensorMap* tm_q, cons
             mbar_arrive_expect_tx(&st.q_full[slot], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
                 tma_load_3d_hint(smem + C::kOffQ + slot * C::kTileBytes + b * C::kBoxBytes, tm_q, &st.q_full[slot],
-                                 64 * b, i * kTile, w.bh, pol_keep);
+                                 64 * b, i * kTile, qbh, pol_keep);
             ++q_loads[slot];
             if (!wait_bar(&st.do_empty[slot], ph, abort_flag)) {
                 ok = false;
@@ -227,7 +243,7 @@ __device__ void run_load(State& st, uint8_t* smem, const CUtensorMap* tm_q, cons
             mbar_arrive_expect_tx(&st.do_full[slot], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
                 tma_load_3d_hint(smem + C::kOffDO + slot * C::kTileBytes + b * C::kBoxBytes, tm_do,
-                                 &st.do_full[slot], 64 * b, i * kTile, w.bh, pol_keep);
+                                 &st.do_full[slot], 64 * b, i * kTile, qbh, pol_keep);
             ++do_loads[slot];
         }
     }
@@ -258,12 +274,13 @@ __device__ void run_stats(State& st, uint8_t* smem, const Params& p) {
         const int idx = tile_index(k, p.n_tiles);
         if (idx < 0) break;
         const Work w = make_work<CAUSAL>(p, idx);
-        const size_t rowbase = static_cast<size_t>(w.bh) * p.N;
-        for (int s = 0; s < w.n; ++s, ++g) {
+        int qi = w.i0, qbh = w.qbh0;
+        for (int s = 0; s < w.n; ++s, ++g, step_next(w, p.T, qi, qbh)) {
             const int stage = g & 1;
             ok = wait_warp(&st.st_empty[stage], ((g >> 1) & 1) ^ 1, abort_flag);
             if (!ok) break;
-            const int q = (w.i0 + s) * kTile + 4 * lane;
+            const size_t rowbase = static_cast<size_t>(qbh) * p.N;
+            const int q = qi * kTile + 4 * lane;
             float a[4], b[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -412,12 +429,13 @@ __device__ void run_compute(State& st, uint8_t* smem, uint32_t tmem, int wg, con
         const Work w = make_work<CAUSAL>(p, idx);
         const int key = w.j * kTile + r;
         const bool key_ok = key < p.N;
-        for (int s = 0; s < w.n; ++s, ++g) {
+        int qi = w.i0, qbh = w.qbh0;
+        for (int s = 0; s < w.n; ++s, ++g, step_next(w, p.T, qi, qbh)) {
             const int stage = g & 1;
             ok = wait_warp(&st.st_full[stage], (g >> 1) & 1, abort_flag) && wait_warp(&st.sp_full, g & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            const bool diag = CAUSAL && (w.i0 + s) == w.j;   // query q sees key r only if r <= q
+            const bool diag = CAUSAL && qi == w.j;   // query q sees key r only if r <= q
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 const int col = 64 * wg + 32 * c;   // first query column of the chunk
@@ -483,7 +501,7 @@ __device__ void run_compute(State& st, uint8_t* smem, uint32_t tmem, int wg, con
         const uint32_t tsrc = tmem + lane_addr + (wg == 0 ? C::kTmDV : C::kTmDK);
         const float mul = wg == 0 ? 1.f : p.scale;
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(wg == 0 ? p.dv : p.dk) +
-                                              (static_cast<size_t>(w.bh) * p.N + (key_ok ? key : 0)) * D);
+                                              (static_cast<size_t>(w.kvbh) * p.N + (key_ok ? key : 0)) * D);
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
             uint32_t v[32];
@@ -540,7 +558,8 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
         const int idx = tile_index(k, p.n_tiles);
         if (idx < 0) break;
         const Work w = make_work<CAUSAL>(p, idx);
-        for (int s = 0; s < w.n; ++s, ++g) {
+        int qi = w.i0, qbh = w.qbh0;
+        for (int s = 0; s < w.n; ++s, ++g, step_next(w, p.T, qi, qbh)) {
             ok = wait_warp(&st.dq_full, g & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
@@ -553,7 +572,8 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&st.dq_free);
-            const int q0 = (w.i0 + s) * kTile;
+            const int q0 = qi * kTile;
+            const size_t qplane = static_cast<size_t>(qbh) * p.N;
             const float sc = p.scale;
             if constexpr (D == 128) {
                 // This thread holds dQ^T for d = 32 quarter + lane and the tile's 128
@@ -564,7 +584,7 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
                 const int nq = p.N - q0 < kTile ? p.N - q0 : kTile;
                 const int i = lane & 3;
                 const bool b0 = (i & 1) != 0, b1 = (i & 2) != 0;
-                float* base = p.dq_acc + (static_cast<size_t>(w.bh) * p.N + q0 + i) * D + 32 * quarter + 4 * (lane >> 2);
+                float* base = p.dq_acc + (qplane + q0 + i) * D + 32 * quarter + 4 * (lane >> 2);
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
 #pragma unroll
@@ -597,7 +617,7 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
                 // 128-byte lines (one piece-row of four groups) instead of 32 pieces.
                 const int b = lane & 7, g = lane >> 3;
                 const int row0 = q0 + 32 * quarter + 8 * g;   // first row of this lane's group
-                float* gbase = p.dq_acc + (static_cast<size_t>(w.bh) * p.N + row0) * D + 4 * b;
+                float* gbase = p.dq_acc + (qplane + row0) * D + 4 * b;
 #pragma unroll
                 for (int c = 0; c < kCols / 32; ++c) {
                     float a[8][4];
@@ -818,10 +838,12 @@ extern "C" size_t fa_bwd_workspace_bytes(int B, int H, int N, int D) {
            bwd::round256(static_cast<size_t>(rows) * sizeof(float));
 }
 
-extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                      void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale, int causal, int dtype,
-                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+extern "C" int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int D,
+                          float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
     if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
@@ -830,6 +852,7 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
     for (const void* ptr : ptrs)
         if (ptr == nullptr || (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0) return FA_ERR_MISALIGNED;
     const uint64_t BH = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
+    const uint64_t BHkv = static_cast<uint64_t>(B) * static_cast<uint64_t>(H_kv);
     const uint64_t rows = BH * static_cast<uint64_t>(N);
     if (BH > 0x7fffffffull || rows * static_cast<uint64_t>(D) >= (uint64_t(1) << 40)) return FA_ERR_INVALID_ARG;
     const uint64_t T = (static_cast<uint64_t>(N) + bwd::kTile - 1) / bwd::kTile;
@@ -837,10 +860,11 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
     const size_t need = fa_bwd_workspace_bytes(B, H, N, D);
     if (need == 0 || workspace_bytes < need) return FA_ERR_INVALID_ARG;
     const size_t tbytes = static_cast<size_t>(rows) * D * 2, lbytes = static_cast<size_t>(rows) * sizeof(float);
+    const size_t kvbytes = static_cast<size_t>(BHkv * N) * D * 2;
     const void* ins[6] = {q, k, v, o, dout, lse};
-    const size_t in_bytes[6] = {tbytes, tbytes, tbytes, tbytes, tbytes, lbytes};
+    const size_t in_bytes[6] = {tbytes, kvbytes, kvbytes, tbytes, tbytes, lbytes};
     const void* outs[4] = {dq, dk, dv, workspace};
-    const size_t out_bytes[4] = {tbytes, tbytes, tbytes, need};
+    const size_t out_bytes[4] = {tbytes, kvbytes, kvbytes, need};
     for (int a = 0; a < 4; ++a) {
         for (int b = 0; b < 6; ++b)
             if (overlaps(outs[a], out_bytes[a], ins[b], in_bytes[b])) return FA_ERR_INVALID_ARG;
@@ -848,9 +872,9 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
             if (overlaps(outs[a], out_bytes[a], outs[b], out_bytes[b])) return FA_ERR_INVALID_ARG;
     }
     CUtensorMap maps[4];
-    const int bh = static_cast<int>(BH);
-    if (!make_tile_map(&maps[0], q, dtype, D, N, bh) || !make_tile_map(&maps[1], k, dtype, D, N, bh) ||
-        !make_tile_map(&maps[2], v, dtype, D, N, bh) || !make_tile_map(&maps[3], dout, dtype, D, N, bh))
+    const int bh = static_cast<int>(BH), bhkv = static_cast<int>(BHkv);
+    if (!make_tile_map(&maps[0], q, dtype, D, N, bh) || !make_tile_map(&maps[1], k, dtype, D, N, bhkv) ||
+        !make_tile_map(&maps[2], v, dtype, D, N, bhkv) || !make_tile_map(&maps[3], dout, dtype, D, N, bh))
         return FA_ERR_CUDA;
     bwd::Params p;
     p.dk = dk;
@@ -861,8 +885,12 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
     p.lse = lse;
     p.N = N;
     p.BH = bh;
+    p.BHkv = bhkv;
+    p.H = H;
+    p.H_kv = H_kv;
+    p.G = H / H_kv;
     p.T = static_cast<int>(T);
-    p.n_tiles = static_cast<int>(T * BH);
+    p.n_tiles = static_cast<int>(T * BHkv);
     p.scale = scale;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     const long long nrows = static_cast<long long>(rows);
@@ -874,4 +902,11 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
         e = dtype == FA_BF16 ? bwd::launch_all<64, true>(maps, p, causal, o, dout, dq, nrows, stream)
                              : bwd::launch_all<64, false>(maps, p, causal, o, dout, dq, nrows, stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                      void* dq, void* dk, void* dv, int B, int H, int N, int D, float scale, int causal, int dtype,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return fa_bwd_gqa(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, N, D, scale, causal, dtype, workspace,
+                      workspace_bytes, stream);
 }

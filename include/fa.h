@@ -303,6 +303,20 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * fa_bwd_gqa -- fa_bwd with grouped key/value heads (the backward pass of
+ * fa_fwd_gqa): q, o, dout, dq are [B,H,N,D] and lse [B,H,N]; k, v, dk, dv are
+ * [B,H_kv,N,D], H a multiple of H_kv, query head h reading K/V head
+ * h / (H / H_kv).  dK and dV of a K/V head sum the contributions of all the
+ * query heads of its group (accumulated in fp32 before the one rounding).
+ * Workspace as for fa_bwd: fa_bwd_workspace_bytes(B, H, N, D).  An H_kv that
+ * does not divide H returns FA_ERR_INVALID_ARG.  fa_bwd is fa_bwd_gqa with
+ * H_kv = H.
+ */
+int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+               void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int D, float scale, int causal,
+               int dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fa_fwd_fp8_host_workspace_bytes -- bytes of device workspace fa_fwd_fp8_host
  * needs: room for Q, K, V^T (B*H*N*D bytes each), the three scale arrays
  * (4*B*H*ceil(N/128) bytes each), O (2*B*H*N*D) and the LSE (4*B*H*N), each

@@ -252,3 +252,10 @@ def test_fp8_host_workspace_size_and_errors(lib):
     assert call(ws=(10 << 20) + 16) == 3
     assert call(wsb=1024) == 1
     assert call() == 1          # fake addresses are not page-locked host memory
+
+
+@pytest.mark.parametrize("H,H_kv,status", [(6, 4, 1), (6, 0, 1), (4, 8, 1)])
+def test_bwd_gqa_head_count_errors(lib, H, H_kv, status):
+    a = dict(BWD)
+    assert fa.fa_bwd_gqa(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"], 1, H, H_kv,
+                         256, 64, 0.125, 1, 0, a["ws"], a["ws_bytes"], 0) == status

@@ -163,3 +163,34 @@ def test_bad_workspace_is_rejected_before_launch():
         fa.attention_backward(q, k, v, o, lse, do, causal=True, workspace=small)
     torch.cuda.synchronize()
     assert fa.fa_get_device_status(0) == fa.FA_OK
+
+
+@pytest.mark.parametrize("H,H_kv", [(8, 2), (6, 3), (4, 1)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D,dtype", [(64, "fp16"), (128, "bf16")])
+@pytest.mark.parametrize("N", [129, 300])
+def test_grouped_kv_heads(N, D, dtype, causal, H, H_kv):
+    """fa_bwd_gqa: the oracle's backward on K/V repeated over each group, with dK
+    and dV of a K/V head the FP64 sum over the query heads that read it."""
+    G = H // H_kv
+    td = torch.float16 if dtype == "fp16" else torch.bfloat16
+    gen = torch.Generator().manual_seed(N + 10 * H + H_kv)
+    q = torch.randn(1, H, N, D, generator=gen).to(td)
+    k = torch.randn(1, H_kv, N, D, generator=gen).to(td)
+    v = torch.randn(1, H_kv, N, D, generator=gen).to(td)
+    do = torch.randn(1, H, N, D, generator=gen).to(td)
+    scale = D ** -0.5
+    qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.attention(qc, kc, vc, causal=causal, scale=scale)
+    dq, dk, dv = fa.attention_backward(qc, kc, vc, o, lse, doc, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status(0) == fa.FA_OK
+    assert dk.shape == k.shape and dv.shape == v.shape
+    e = "f16" if dtype == "fp16" else "bf16"
+    kr, vr = (t.repeat_interleave(G, dim=1) for t in (k, v))
+    rq, rk, rv, _ = fa_ref.backward(*(fa_inputs.bits(t) for t in (q, kr, vr, do)), scale, causal, enc=e)
+    rk = rk.reshape(1, H_kv, G, N, D).sum(axis=2)
+    rv = rv.reshape(1, H_kv, G, N, D).sum(axis=2)
+    what = "H%d/%d N=%d D=%d causal=%d" % (H, H_kv, N, D, causal)
+    for name, g_, r_ in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        _check(name, g_, r_, dtype, what)
