@@ -194,3 +194,41 @@ def test_grouped_kv_heads(N, D, dtype, causal, H, H_kv):
     what = "H%d/%d N=%d D=%d causal=%d" % (H, H_kv, N, D, causal)
     for name, g_, r_ in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
         _check(name, g_, r_, dtype, what)
+
+
+def test_grouped_kv_heads_full_size_sampled():
+    """B1 H32 H_kv 8 N4096 D128 causal fp16 (four query heads per K/V head, 32
+    Q tiles each): sampled dQ rows, and sampled dK / dV keys whose reference is
+    the FP64 sum over the group of the oracle's per-head gradients on repeated
+    K/V."""
+    B, H, H_kv, N, D, G = 1, 32, 8, 4096, 128, 4
+    gen = torch.Generator().manual_seed(5)
+    q = torch.randn(B, H, N, D, generator=gen).half()
+    k = torch.randn(B, H_kv, N, D, generator=gen).half()
+    v = torch.randn(B, H_kv, N, D, generator=gen).half()
+    do = torch.randn(B, H, N, D, generator=gen).half()
+    scale = D ** -0.5
+    qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.attention(qc, kc, vc, causal=True, scale=scale)
+    dq, dk, dv = fa.attention_backward(qc, kc, vc, o, lse, doc, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status(0) == fa.FA_OK
+    rng = np.random.default_rng(3)
+    rows = np.concatenate([[0, 127, 128, N - 1], rng.integers(0, N, 28)])
+    bh_q = rng.integers(0, B * H, rows.size)
+    kv_heads = np.array([0, 3, B * H_kv - 1])
+    keys = np.concatenate([[0, 1, 128, N - 1], rng.integers(0, N, 12)])
+    kvh = np.repeat(kv_heads, keys.size)
+    keys = np.tile(keys, kv_heads.size)
+    # each K/V head's gradient is the sum over its G query heads on repeated K/V
+    bh_k = (kvh[:, None] * G + np.arange(G)[None, :]).reshape(-1)
+    keys_rep = np.repeat(keys, G)
+    kr, vr = (t.repeat_interleave(G, dim=1) for t in (k, v))
+    rq, rk, rv = fa_ref.backward_sample(*(fa_inputs.bits(t) for t in (q, kr, vr, do)), scale, True,
+                                        bh_q, rows, bh_k, keys_rep, enc="f16")
+    rk = rk.reshape(-1, G, D).sum(axis=1)
+    rv = rv.reshape(-1, G, D).sum(axis=1)
+    sel = lambda t, a, b: t.reshape(-1, N, D)[torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()]
+    _check("dQ", sel(dq, bh_q, rows), rq, "fp16", "GQA full size")
+    _check("dK", sel(dk, kvh, keys), rk, "fp16", "GQA full size")
+    _check("dV", sel(dv, kvh, keys), rv, "fp16", "GQA full size")
