@@ -70,7 +70,8 @@ struct __align__(8) State {
     uint64_t q_full[2], q_empty[2];             // Q_i ring
     uint64_t do_full[2], do_empty[2];           // dO_i ring
     uint64_t st_full[2], st_empty[2];           // LSE / Delta stages
-    uint64_t sp_full;                           // S^T and dP^T of the step are in TMEM
+    uint64_t s_full, dp_full;                   // S^T / dP^T of the step in TMEM (D = 128: both, on s_full)
+    uint64_t p_ready;                           // P^T in TMEM (D = 64; 8 compute warps)
     uint64_t pds_ready;                         // P^T, dS^T in TMEM and dS^T in smem (8 compute warps)
     uint64_t dq_full, dq_free;                  // dQ^T in TMEM / read out (4 dQ warps)
     uint64_t dkv_full, dkv_free;                // dK, dV of the work tile complete / read out
@@ -92,9 +93,15 @@ struct Cfg {
     static constexpr int kOffStats = kOffDS + 2 * kBoxBytes;   // lse2[2][128], delta[2][128] fp32
     static constexpr int kOffState = kOffStats + 4 * kTile * 4;
     static constexpr int kSmemBytes = kOffState + static_cast<int>(sizeof(State));
+    // Step order.  D = 64 issues S^T first and splits the compute pass: P (from
+    // S^T alone) goes to TMEM and dV starts on it while dS waits for dP^T; dQ
+    // then takes the dP^T / dS^T columns.  D = 128 issues dP^T first, computes P
+    // and dS in one pass, and puts dQ^T over S^T / P^T (measured faster there).
+    static constexpr bool kEarlyP = D == 64;
     // TMEM columns
-    static constexpr uint32_t kTmA = 0;          // S^T -> P^T (16-bit) -> dQ^T
-    static constexpr uint32_t kTmB = 128;        // dP^T -> dS^T (16-bit)
+    static constexpr uint32_t kTmA = 0;          // S^T -> P^T (16-bit) [-> dQ^T, D = 128]
+    static constexpr uint32_t kTmB = 128;        // dP^T -> dS^T (16-bit) [-> dQ, D = 64]
+    static constexpr uint32_t kTmDQ = kEarlyP ? kTmB : kTmA;
     static constexpr uint32_t kTmDV = 256;
     static constexpr uint32_t kTmDK = 256 + D;
 };
@@ -297,8 +304,10 @@ __device__ void run_stats(State& st, uint8_t* smem, const Params& p) {
 }
 
 // UMMA issuer: warp 1, all lanes run the control flow, one elected lane issues.
-// Per step: dP^T = V_j dO_i^T, S^T = K_j Q_i^T; then, once the compute warps
-// have written P^T / dS^T: dV += P^T dO_i, dK += dS^T Q_i, dQ^T = K_j^T dS^T.
+// Per step: S^T = K_j Q_i^T and dP^T = V_j dO_i^T; dV += P^T dO_i once the
+// compute warps have written P^T, dK += dS^T Q_i once they have written dS^T,
+// then dQ^T = K_j^T dS^T (D = 128) or dQ = dS K_j (D = 64).  Cfg::kEarlyP sets
+// the order of S^T and dP^T and where dQ goes in TMEM.
 template <int D, bool BF16, bool CAUSAL>
 __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p) {
     using C = Cfg<D>;
@@ -346,27 +355,58 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
         for (int s = 0; s < w.n; ++s, ++g) {
             const int slot = g & 1;
             const uint32_t ph = (g >> 1) & 1;
-            if (!wait_warp(&st.do_full[slot], ph, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
+            if constexpr (C::kEarlyP) {
+                // S^T first: its columns were last read by the previous step's dV,
+                // issued before it, so it waits only for Q.
+                if (!wait_warp(&st.q_full[slot], ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kSteps; ++kk)
-                umma_ss_elect(tmem + C::kTmB, dV + koff(kk), dDOk[slot] + koff(kk), kIdS, kk > 0);
-            if ((g > 0 && !wait_warp(&st.dq_free, (g - 1) & 1, abort_flag)) ||
-                !wait_warp(&st.q_full[slot], ph, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
+                for (int kk = 0; kk < kSteps; ++kk)
+                    umma_ss_elect(tmem + C::kTmA, dK + koff(kk), dQk[slot] + koff(kk), kIdS, kk > 0);
+                umma_commit_elect(&st.s_full);
+                // dP^T into the columns of the previous step's dQ, once that has been read out
+                if (!wait_warp(&st.do_full[slot], ph, abort_flag) ||
+                    (g > 0 && !wait_warp(&st.dq_free, (g - 1) & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < kSteps; ++kk)
-                umma_ss_elect(tmem + C::kTmA, dK + koff(kk), dQk[slot] + koff(kk), kIdS, kk > 0);
-            umma_commit_elect(&st.sp_full);
-            if (!wait_warp(&st.pds_ready, g & 1, abort_flag)) {
-                ok = false;
-                break;
+                for (int kk = 0; kk < kSteps; ++kk)
+                    umma_ss_elect(tmem + C::kTmB, dV + koff(kk), dDOk[slot] + koff(kk), kIdS, kk > 0);
+                umma_commit_elect(&st.dp_full);
+                // dV as soon as P^T is in TMEM, while the compute warps work on dS^T
+                if (!wait_warp(&st.p_ready, g & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+            } else {
+                if (!wait_warp(&st.do_full[slot], ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kSteps; ++kk)
+                    umma_ss_elect(tmem + C::kTmB, dV + koff(kk), dDOk[slot] + koff(kk), kIdS, kk > 0);
+                // S^T into the columns of the previous step's dQ^T, once that has been read out
+                if ((g > 0 && !wait_warp(&st.dq_free, (g - 1) & 1, abort_flag)) ||
+                    !wait_warp(&st.q_full[slot], ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kSteps; ++kk)
+                    umma_ss_elect(tmem + C::kTmA, dK + koff(kk), dQk[slot] + koff(kk), kIdS, kk > 0);
+                umma_commit_elect(&st.s_full);   // S^T and dP^T
+                if (!wait_warp(&st.pds_ready, g & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
             }
             tc_fence_after();
             // K-step kk over the queries reads 16 rows = 2048 bytes of dO / Q (MN-major)
@@ -375,19 +415,27 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
                 umma_ts_elect(tmem + C::kTmDV, tmem + C::kTmA + acol(kk), dDOmn[slot] + 128 * kk, kIdG,
                               (s > 0 || kk > 0) ? 1u : 0u);
             umma_commit_elect(&st.do_empty[slot]);
+            if constexpr (C::kEarlyP) {
+                if (!wait_warp(&st.pds_ready, g & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
                 umma_ts_elect(tmem + C::kTmDK, tmem + C::kTmB + acol(kk), dQmn[slot] + 128 * kk, kIdG,
                               (s > 0 || kk > 0) ? 1u : 0u);
             umma_commit_elect(&st.q_empty[slot]);
-            // dQ^T = K^T dS^T (D = 128) or dQ = dS K (D = 64): K-step kk over the keys reads 16
-            // rows of K and of dS^T, both stored with the M or N index contiguous (MN-major)
+            // dQ^T = K^T dS^T (D = 128) or dQ = dS K (D = 64), after dK (and dV) have read
+            // the TMEM columns it overwrites: K-step kk over the keys reads 16 rows of K
+            // and of dS^T in smem, both stored with the M or N index contiguous (MN-major)
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
                 if constexpr (D == 128)
-                    umma_ss_elect(tmem + C::kTmA, dKmn + 128 * kk, dDSmn + 128 * kk, kIdQ, kk > 0);
+                    umma_ss_elect(tmem + C::kTmDQ, dKmn + 128 * kk, dDSmn + 128 * kk, kIdQ, kk > 0);
                 else
-                    umma_ss_elect(tmem + C::kTmA, dDSmn + 128 * kk, dKmn + 128 * kk, kIdQ, kk > 0);
+                    umma_ss_elect(tmem + C::kTmDQ, dDSmn + 128 * kk, dKmn + 128 * kk, kIdQ, kk > 0);
             }
             umma_commit_elect(&st.dq_full);
         }
@@ -432,56 +480,129 @@ __device__ void run_compute(State& st, uint8_t* smem, uint32_t tmem, int wg, con
         int qi = w.i0, qbh = w.qbh0;
         for (int s = 0; s < w.n; ++s, ++g, step_next(w, p.T, qi, qbh)) {
             const int stage = g & 1;
-            ok = wait_warp(&st.st_full[stage], (g >> 1) & 1, abort_flag) && wait_warp(&st.sp_full, g & 1, abort_flag);
+            ok = wait_warp(&st.st_full[stage], (g >> 1) & 1, abort_flag) && wait_warp(&st.s_full, g & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
             const bool diag = CAUSAL && qi == w.j;   // query q sees key r only if r <= q
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                const int col = 64 * wg + 32 * c;   // first query column of the chunk
-                uint32_t sv[32], dv[32];
-                tmem_ld32_nowait(tA + col, sv);
-                tmem_ld32_nowait(tB + col, dv);
-                tmem_ld_wait_regs(sv);
-                regs_after_wait(dv);
-                const float4* L = reinterpret_cast<const float4*>(lse2s + stage * kTile + col);
-                const float4* Dl = reinterpret_cast<const float4*>(dls + stage * kTile + col);
-                uint32_t pp[16], dd[16];
+            if constexpr (C::kEarlyP) {
+                // P first, from S^T alone (dP^T may still be in the tensor core): P^T to
+                // TMEM for dV, the fp32 p kept in registers for dS.
+                float pk[2][32];
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 l4 = L[e / 4], d4 = Dl[e / 4];
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pv[4], dsv[4];
+                for (int c = 0; c < 2; ++c) {
+                    const int col = 64 * wg + 32 * c;   // first query column of the chunk
+                    uint32_t sv[32];
+                    tmem_ld32_wait(tA + col, sv);
+                    const float4* L = reinterpret_cast<const float4*>(lse2s + stage * kTile + col);
+                    uint32_t pp[16];
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        float pr = ex2_approx(fmaf(__uint_as_float(sv[e + h]), c_log2, -lv[h]));
-                        if (!key_ok || (diag && r > col + e + h)) pr = 0.f;
-                        pv[h] = pr;
-                        dsv[h] = pr * (__uint_as_float(dv[e + h]) - dl[h]);
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 l4 = L[e / 4];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            float pr = ex2_approx(fmaf(__uint_as_float(sv[e + h]), c_log2, -lv[h]));
+                            if (!key_ok || (diag && r > col + e + h)) pr = 0.f;
+                            pk[c][e + h] = pr;
+                        }
+                        if constexpr (BF16) {
+                            pp[e / 2] = pack_bf16x2(pk[c][e], pk[c][e + 1]);
+                            pp[e / 2 + 1] = pack_bf16x2(pk[c][e + 2], pk[c][e + 3]);
+                        } else {
+                            pp[e / 2] = pack_f16x2(pk[c][e], pk[c][e + 1]);
+                            pp[e / 2 + 1] = pack_f16x2(pk[c][e + 2], pk[c][e + 3]);
+                        }
                     }
-                    if constexpr (BF16) {
-                        pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
-                        pp[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
-                        dd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
-                        dd[e / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
-                    } else {
-                        pp[e / 2] = pack_f16x2(pv[0], pv[1]);
-                        pp[e / 2 + 1] = pack_f16x2(pv[2], pv[3]);
-                        dd[e / 2] = pack_f16x2(dsv[0], dsv[1]);
-                        dd[e / 2 + 1] = pack_f16x2(dsv[2], dsv[3]);
+                    // P^T of these 32 queries: 16 packed columns inside the chunk's own
+                    // (already read) columns -- 64*wg + 16*c is below col + 32 for c = 0 and 1.
+                    tmem_st16(tA + 64 * wg + 16 * c, pp);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&st.p_ready);
+                ok = wait_warp(&st.dp_full, g & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int col = 64 * wg + 32 * c;
+                    uint32_t dv[32];
+                    tmem_ld32_wait(tB + col, dv);
+                    const float4* Dl = reinterpret_cast<const float4*>(dls + stage * kTile + col);
+                    uint32_t dd[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 d4 = Dl[e / 4];
+                        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float dsv[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) dsv[h] = pk[c][e + h] * (__uint_as_float(dv[e + h]) - dl[h]);
+                        if constexpr (BF16) {
+                            dd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+                            dd[e / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+                        } else {
+                            dd[e / 2] = pack_f16x2(dsv[0], dsv[1]);
+                            dd[e / 2 + 1] = pack_f16x2(dsv[2], dsv[3]);
+                        }
+                    }
+                    tmem_st16(tB + 64 * wg + 16 * c, dd);
+                    // dS^T row r, queries 32c .. 32c+31 of box wg: 16-byte chunks 4c .. 4c+3, swizzled
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint32_t chunk = static_cast<uint32_t>(4 * c + cc);
+                        st_shared_v4(ds_row + ((chunk ^ sw) << 4), dd[4 * cc], dd[4 * cc + 1], dd[4 * cc + 2],
+                                     dd[4 * cc + 3]);
                     }
                 }
-                // P^T / dS^T of these 32 queries: 16 packed columns inside the chunk's own
-                // (already read) columns -- 64*wg + 16*c is below col + 32 for c = 0 and 1.
-                tmem_st16(tA + 64 * wg + 16 * c, pp);
-                tmem_st16(tB + 64 * wg + 16 * c, dd);
-                // dS^T row r, queries 32c .. 32c+31 of box wg: 16-byte chunks 4c .. 4c+3, swizzled
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    const int col = 64 * wg + 32 * c;   // first query column of the chunk
+                    uint32_t sv[32], dv[32];
+                    tmem_ld32_nowait(tA + col, sv);
+                    tmem_ld32_nowait(tB + col, dv);
+                    tmem_ld_wait_regs(sv);
+                    regs_after_wait(dv);
+                    const float4* L = reinterpret_cast<const float4*>(lse2s + stage * kTile + col);
+                    const float4* Dl = reinterpret_cast<const float4*>(dls + stage * kTile + col);
+                    uint32_t pp[16], dd[16];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    const uint32_t chunk = static_cast<uint32_t>(4 * c + cc);
-                    st_shared_v4(ds_row + ((chunk ^ sw) << 4), dd[4 * cc], dd[4 * cc + 1], dd[4 * cc + 2],
-                                 dd[4 * cc + 3]);
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 l4 = L[e / 4], d4 = Dl[e / 4];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pv[4], dsv[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            float pr = ex2_approx(fmaf(__uint_as_float(sv[e + h]), c_log2, -lv[h]));
+                            if (!key_ok || (diag && r > col + e + h)) pr = 0.f;
+                            pv[h] = pr;
+                            dsv[h] = pr * (__uint_as_float(dv[e + h]) - dl[h]);
+                        }
+                        if constexpr (BF16) {
+                            pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
+                            pp[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+                            dd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
+                            dd[e / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
+                        } else {
+                            pp[e / 2] = pack_f16x2(pv[0], pv[1]);
+                            pp[e / 2 + 1] = pack_f16x2(pv[2], pv[3]);
+                            dd[e / 2] = pack_f16x2(dsv[0], dsv[1]);
+                            dd[e / 2 + 1] = pack_f16x2(dsv[2], dsv[3]);
+                        }
+                    }
+                    // P^T / dS^T of these 32 queries: 16 packed columns inside the chunk's own
+                    // (already read) columns -- 64*wg + 16*c is below col + 32 for c = 0 and 1.
+                    tmem_st16(tA + 64 * wg + 16 * c, pp);
+                    tmem_st16(tB + 64 * wg + 16 * c, dd);
+                    // dS^T row r, queries 32c .. 32c+31 of box wg: 16-byte chunks 4c .. 4c+3, swizzled
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint32_t chunk = static_cast<uint32_t>(4 * c + cc);
+                        st_shared_v4(ds_row + ((chunk ^ sw) << 4), dd[4 * cc], dd[4 * cc + 1], dd[4 * cc + 2],
+                                     dd[4 * cc + 3]);
+                    }
                 }
             }
             tmem_st_wait();
@@ -550,7 +671,7 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
     volatile int* abort_flag = &st.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
     // TMEM lane 32 quarter + lane: head-dim index d (D = 128) or query row (D = 64)
-    const uint32_t tA = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + C::kTmA;
+    const uint32_t tA = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + C::kTmDQ;
     constexpr int kCols = D == 128 ? kTile : D;   // TMEM columns of the step's dQ
     int g = 0;
     bool ok = true;
@@ -678,7 +799,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&st.st_full[s], 32);
             mbar_init(&st.st_empty[s], 8);
         }
-        mbar_init(&st.sp_full, 1);
+        mbar_init(&st.s_full, 1);
+        mbar_init(&st.dp_full, 1);
+        mbar_init(&st.p_ready, 8);
         mbar_init(&st.pds_ready, 8);
         mbar_init(&st.dq_full, 1);
         mbar_init(&st.dq_free, 4);
