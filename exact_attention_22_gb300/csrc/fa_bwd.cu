@@ -455,6 +455,9 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
 //   p = 2^(S^T * scale * log2 e - LSE_q * log2 e), 0 where masked,
 //   ds = p (dP^T - Delta_q),
 // P^T and dS^T packed to 16 bits back into TMEM, dS^T also into shared memory.
+// D = 128 takes p and ds in one pass once S^T and dP^T are both in TMEM; D = 64
+// first writes P^T (signalling p_ready, so dV can start) with p kept in
+// registers, then waits for dP^T and writes dS^T.
 // At the end of a work tile wg 0 writes the dV rows, wg 1 the dK rows.
 template <int D, bool BF16, bool CAUSAL>
 __device__ void run_compute(State& st, uint8_t* smem, uint32_t tmem, int wg, const Params& p) {
