@@ -3,6 +3,7 @@ include/fa.h declares, and rejects bad arguments before touching CUDA."""
 import math
 import os
 import re
+import shutil
 import subprocess
 
 import pytest
@@ -259,3 +260,41 @@ def test_bwd_gqa_head_count_errors(lib, H, H_kv, status):
     a = dict(BWD)
     assert fa.fa_bwd_gqa(a["q"], a["k"], a["v"], a["o"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"], 1, H, H_kv,
                          256, 64, 0.125, 1, 0, a["ws"], a["ws_bytes"], 0) == status
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "fa.h"
+
+int main(void) {
+    size_t ws = fa_splitkv_workspace_bytes(1, 2, 256, 64, 4);
+    size_t bw = fa_bwd_workspace_bytes(1, 2, 256, 64);
+    int st = fa_fwd(NULL, NULL, NULL, NULL, NULL, 0, 2, 256, 64, 0.125f, 0, FA_FP16, (cudaStream_t)0);
+    int st2 = fa_fwd((void*)16, (void*)32, (void*)48, (void*)64, (float*)80, 1, 2, 256, 96, 0.125f, 0, FA_FP16,
+                     (cudaStream_t)0);
+    printf("%zu %zu %d %d %s\n", ws, bw, st, st2, fa_status_string(st));
+    return 0;
+}
+"""
+
+
+def test_header_is_plain_c(lib, tmp_path):
+    """include/fa.h compiles as C99 with warnings as errors, and a C program
+    linked against the library gets the sizes and argument errors the binding
+    sees (both returned before anything reaches CUDA)."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "prog.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "prog"
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    libpath = fa.library_path()
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), "-I",
+                    cuda_inc, str(src), libpath, "-Wl,-rpath," + os.path.dirname(libpath), "-o", str(exe)],
+                   check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == fa.fa_splitkv_workspace_bytes(1, 2, 256, 64, 4)
+    assert int(out[1]) == fa.fa_bwd_workspace_bytes(1, 2, 256, 64)
+    assert int(out[2]) == 1 and out[4] == "FA_ERR_INVALID_ARG"   # B = 0
+    assert int(out[3]) == 2                                     # D = 96: unsupported
