@@ -144,8 +144,11 @@ def test_full_size_sampled(name):
     assert sv < 1e-2, "sum_j dV_j vs sum_i dO_i: %.3e" % sv
 
 
-def test_dk_dv_deterministic_dq_close():
-    w = fa_inputs.WORKLOADS["causal_fp16_b1h32n1024d128"]
+@pytest.mark.parametrize("D", [128, 64])
+def test_dk_dv_deterministic_dq_close(D):
+    """dK and dV are summed in TMEM in a fixed order (D = 128 in one compute pass,
+    D = 64 with P and dS in two), so two runs give the same bits."""
+    w = fa_inputs.Workload("det", 1, 32, 1024, D, True, "fp16")
     q, k, v, do = _inputs(w, seed=4)
     a = _gpu_grads(q, k, v, do, True, w.scale)
     b = _gpu_grads(q, k, v, do, True, w.scale)
