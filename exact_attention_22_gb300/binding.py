@@ -29,6 +29,40 @@ class FaError(RuntimeError):
         self.status = status
 
 
+def _check_given(t, shape, dtype, name, device=None, pinned=False):
+    """A caller-provided output must be exactly what the kernel writes: its
+    shape and dtype, contiguous, and on the inputs' device (or page-locked host
+    memory for the host entry points).  The C ABI sees only a pointer."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError("%s must be %s %s" % (name, dtype, list(shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if pinned:
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError("%s must be a page-locked host tensor" % name)
+    elif t.device != device:
+        raise ValueError("%s must be on %s" % (name, device))
+
+
+def _check_workspace(ws, device):
+    """A caller-provided workspace: contiguous bytes on the given CUDA device
+    (its size is checked by the library)."""
+    if ws is None:
+        return
+    if not ws.is_cuda or ws.device != device or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous tensor on %s" % device)
+
+
+def _same_device(ts):
+    """Every tensor of a device call on one GPU: a pointer from another device
+    would reach the kernel."""
+    dev = ts[0].device
+    if any(t.device != dev for t in ts[1:]):
+        raise ValueError("all tensors must be on one device (%s)" % dev)
+
+
 def library_path() -> str:
     return _LIB_PATH
 
@@ -242,7 +276,11 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, out=Non
     for t in (q, k, v):
         if not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous")
+    _same_device((q, k, v))
     B, H, N, D = q.shape
+    _check_given(out, q.shape, q.dtype, "out", q.device)
+    _check_given(lse, (B, H, N), torch.float32, "lse", q.device)
+    _check_workspace(workspace, q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -299,9 +337,12 @@ def attention_host(q, k, v, causal: bool = False, scale: float | None = None, ou
     if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
         raise ValueError("q, k, v must all be [B, H, N, D]")
     B, H, N, D = q.shape
+    _check_given(out, q.shape, q.dtype, "out", pinned=True)
+    _check_given(lse, (B, H, N), torch.float32, "lse", pinned=True)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check_workspace(workspace, device)
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
     if lse is None:
@@ -349,6 +390,9 @@ def attention_backward_host(q, k, v, out, lse, dout, causal: bool = False, scale
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    for g, name in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check_given(g, q.shape, q.dtype, name, pinned=True)
+    _check_workspace(workspace, device)
     dq, dk, dv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) if g is None else g for g in (dq, dk, dv))
     need = fa_bwd_host_workspace_bytes(B, H, N, D)
     if workspace is None:
@@ -392,6 +436,11 @@ def attention_backward(q, k, v, out, lse, dout, causal: bool = False, scale: flo
         raise ValueError("lse must be float32 [B, H, N]")
     if not all(t.is_contiguous() for t in ts + (lse,)):
         raise ValueError("inputs must be contiguous")
+    _same_device(ts + (lse,))
+    _check_given(dq, q.shape, q.dtype, "dq", q.device)
+    _check_given(dk, k.shape, q.dtype, "dk", q.device)
+    _check_given(dv, k.shape, q.dtype, "dv", q.device)
+    _check_workspace(workspace, q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     dq = torch.empty_like(q) if dq is None else dq
@@ -432,6 +481,9 @@ def attention_fp8(q8, k8, v8_t, q_scale, k_scale, v_scale, causal: bool = False,
     for t in (q_scale, k_scale, v_scale):
         if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and tuple(t.shape) == (B, H, nb)):
             raise ValueError("scales must be contiguous float32 CUDA tensors [B, H, ceil(N/128)]")
+    _same_device(ts + (q_scale, k_scale, v_scale))
+    _check_given(out, (B, H, N, D), torch.bfloat16, "out", q8.device)
+    _check_given(lse, (B, H, N), torch.float32, "lse", q8.device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -464,8 +516,12 @@ def attention_kv(q, k, v, causal: bool = False, scale: float | None = None, num_
         raise ValueError("q must be [B, H, Nq, D] and k, v [B, H_kv, Nk, D]")
     if not all(t.is_contiguous() for t in (q, k, v)):
         raise ValueError("q, k, v must be contiguous")
+    _same_device((q, k, v))
     B, H, Nq, D = q.shape
     H_kv, Nk = k.shape[1], k.shape[2]
+    _check_given(out, q.shape, q.dtype, "out", q.device)
+    _check_given(lse, (B, H, Nq), torch.float32, "lse", q.device)
+    _check_workspace(workspace, q.device)
     if num_splits == "auto":
         with torch.cuda.device(q.device):
             num_splits = fa_fwd_kv_splits_hint(B, H, H_kv, Nq, Nk, D, int(bool(causal)))

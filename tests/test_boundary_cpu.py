@@ -298,3 +298,25 @@ def test_header_is_plain_c(lib, tmp_path):
     assert int(out[1]) == fa.fa_bwd_workspace_bytes(1, 2, 256, 64)
     assert int(out[2]) == 1 and out[4] == "FA_ERR_INVALID_ARG"   # B = 0
     assert int(out[3]) == 2                                     # D = 96: unsupported
+
+
+def test_wrapper_output_checks():
+    """The wrappers' checks of caller-provided outputs and workspaces (the C ABI
+    sees only pointers): exact shape and dtype, contiguous, right device or
+    page-locked memory; a workspace must be device memory."""
+    import torch
+    from exact_attention_22_gb300 import binding as b
+
+    cpu = torch.device("cpu")
+    t = torch.empty(2, 3, 4)
+    b._check_given(None, (9,), torch.float16, "out", cpu)
+    b._check_given(t, (2, 3, 4), torch.float32, "out", cpu)
+    for bad, shape, dtype in ((t, (2, 3, 5), torch.float32), (t, (2, 3, 4), torch.float16),
+                              (t.transpose(0, 1), (3, 2, 4), torch.float32)):
+        with pytest.raises(ValueError, match="out"):
+            b._check_given(bad, shape, dtype, "out", cpu)
+    with pytest.raises(ValueError, match="lse"):
+        b._check_given(t, (2, 3, 4), torch.float32, "lse", pinned=True)   # pageable host memory
+    with pytest.raises(ValueError, match="workspace"):
+        b._check_workspace(torch.empty(16, dtype=torch.uint8), cpu)
+    b._same_device((t, t))
