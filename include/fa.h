@@ -1,5 +1,10 @@
 /*
- * fa.h -- C ABI of the exact attention forward pass on sm_103a (GB300).
+ * fa.h -- C ABI of exact attention on sm_103a (GB300): the forward pass
+ * (fa_fwd; grouped K/V heads fa_fwd_gqa; split-K fa_fwd_splitkv and
+ * fa_fwd_splitkv_noalloc; queries against a longer key sequence, as in
+ * decoding, fa_fwd_kv; E4M3 inputs fa_fwd_fp8), the backward pass (fa_bwd,
+ * fa_bwd_gqa), the same passes on page-locked host tensors (fa_fwd_host,
+ * fa_fwd_fp8_host, fa_bwd_host), and the status calls.
  *
  * The operation ("CUDA FlashAttention: from online softmax to the
  * long-sequence IO limit", sections 1 and 4; "Why FlashAttention does not
