@@ -223,8 +223,8 @@ def run_reference(args, w):
         rows += r
         secs += s
     value = statistics.median(vals)
-    sample = "%d query rows drawn at random from all %d rows of the workload, %.1f s of FP64 oracle time" % (
-        rows, w.B * w.H * w.N, secs)
+    sample = ("%d query rows drawn uniformly at random (with replacement) from all %d rows of the workload, "
+              "%.1f s of FP64 oracle time" % (rows, w.B * w.H * w.N, secs))
     line = {
         "impl": "reference", "metric": "attention fwd TFLOP/s (causal-adjusted)", "value": value,
         "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -419,8 +419,8 @@ def run_ours(args, w):
         tf1, rows1, secs1, _, _ = cpu_oracle_sample(w, seconds=min(3.0, args.cpu_seconds), nthreads=1)
         line["cpu_baseline"] = {
             "value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": "%d query rows drawn at random from the workload's %d rows, naive FP64 oracle, %.1f s"
-                      % (rows, w.B * w.H * w.N, secs),
+            "sample": ("%d query rows drawn uniformly at random (with replacement) from the workload's %d rows, "
+                       "naive FP64 oracle, %.1f s" % (rows, w.B * w.H * w.N, secs)),
             "one_thread": {"value": tf1, "unit": "TFLOP/s", "sample": "the first %d rows of the same sample, "
                            "%.1f s" % (rows1, secs1)}}
     if rank == 0:
