@@ -29,7 +29,7 @@ constexpr long long kMinChunkTiles = 128;
 struct HostIo {
     bool ready = false;
     cudaStream_t h2d = nullptr, d2h = nullptr;
-    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr, in_done = nullptr;
     cudaEvent_t in[kMaxChunks] = {}, out[kMaxChunks] = {};
 };
 
@@ -44,12 +44,13 @@ int io_state(int dev, HostIo** out) {
         bool ok = cudaStreamCreateWithFlags(&s.h2d, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaStreamCreateWithFlags(&s.d2h, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaEventCreateWithFlags(&s.start, ev) == cudaSuccess &&
-                  cudaEventCreateWithFlags(&s.done, ev) == cudaSuccess;
+                  cudaEventCreateWithFlags(&s.done, ev) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&s.in_done, ev) == cudaSuccess;
         for (int c = 0; ok && c < kMaxChunks; ++c)
             ok = cudaEventCreateWithFlags(&s.in[c], ev) == cudaSuccess &&
                  cudaEventCreateWithFlags(&s.out[c], ev) == cudaSuccess;
         if (!ok) {   // undo, so that a later call starts from nothing
-            for (cudaEvent_t* e : {&s.start, &s.done})
+            for (cudaEvent_t* e : {&s.start, &s.done, &s.in_done})
                 if (*e) cudaEventDestroy(*e), *e = nullptr;
             for (int c = 0; c < kMaxChunks; ++c) {
                 if (s.in[c]) cudaEventDestroy(s.in[c]), s.in[c] = nullptr;
@@ -113,10 +114,13 @@ bool pipeline_begin(HostIo* io, cudaStream_t stream) {
            cudaStreamWaitEvent(io->d2h, io->start, 0) == cudaSuccess;
 }
 
-// `stream` ordered after every copy back, also after an error part-way
-// through (what was queued still completes before later work).
+// `stream` ordered after every copy in both directions, also after an error
+// part-way through: a chunk's inputs may be queued when its kernel fails to
+// launch, and those copies still use the caller's buffers.
 bool pipeline_end(HostIo* io, cudaStream_t stream) {
-    return cudaEventRecord(io->done, io->d2h) == cudaSuccess && cudaStreamWaitEvent(stream, io->done, 0) == cudaSuccess;
+    return cudaEventRecord(io->in_done, io->h2d) == cudaSuccess &&
+           cudaStreamWaitEvent(stream, io->in_done, 0) == cudaSuccess &&
+           cudaEventRecord(io->done, io->d2h) == cudaSuccess && cudaStreamWaitEvent(stream, io->done, 0) == cudaSuccess;
 }
 
 // Device workspace: Q, K, V, O ([B,H,N,D] 16-bit each), then LSE ([B,H,N] fp32).
