@@ -253,9 +253,11 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int N, int D);
  *               are back in host memory; returns without waiting
  *
  * Returns FA_OK once everything is queued; synchronise `stream` before
- * reading o or lse.  Pageable or managed host memory, a workspace that is not
- * device memory or is too small, and outputs that overlap inputs give
- * FA_ERR_INVALID_ARG before anything is queued; other argument rules and codes
+ * reading o or lse.  If a CUDA call fails part-way (FA_ERR_CUDA), the copies
+ * already queued still finish before later work on `stream` starts.
+ * Pageable or managed host memory, a workspace that is not device memory or
+ * is too small, and outputs that overlap inputs give FA_ERR_INVALID_ARG
+ * before anything is queued; other argument rules and codes
  * are those of fa_fwd.  Calls from several host threads are serialised while
  * they queue work; calls that may run at the same time on the GPU must not
  * share a workspace.
