@@ -13,5 +13,6 @@ from .binding import (FA_BF16, FA_FP16, FA_OK, FaError, STATUS_NAMES, attention,
                       fa_fwd_kv_workspace_bytes,
                       fa_fwd_splitkv,
                       fa_fwd_splitkv_noalloc,
-                      fa_get_device_status, fa_noalloc_scratch_bytes, fa_selftest_wait_timeout,
+                      fa_get_device_status, fa_noalloc_scratch_bytes, fa_selftest_bwd_fault, fa_selftest_fwd_fault,
+                      fa_selftest_wait_timeout,
                       fa_splitkv_workspace_bytes, fa_status_string, library_path, load_library)

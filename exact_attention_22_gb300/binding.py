@@ -92,6 +92,10 @@ def load_library():
         lib.fa_noalloc_scratch_bytes.restype = ctypes.c_size_t
         lib.fa_selftest_wait_timeout.argtypes = [vp]
         lib.fa_selftest_wait_timeout.restype = I
+        lib.fa_selftest_fwd_fault.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, F, I, I, I, vp]
+        lib.fa_selftest_fwd_fault.restype = I
+        lib.fa_selftest_bwd_fault.argtypes = [vp] * 9 + [I, I, I, I, F, I, I, vp, ctypes.c_size_t, I, vp]
+        lib.fa_selftest_bwd_fault.restype = I
         lib.fa_fwd_kv_workspace_bytes.argtypes = [I, I, I, I, I]
         lib.fa_fwd_kv_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_fwd_kv.argtypes = [vp, vp, vp, vp, vp, I, I, I, I, I, I, F, I, I, I, vp, ctypes.c_size_t, vp]
@@ -246,6 +250,24 @@ def fa_get_device_status(stream: int) -> int:
 def fa_selftest_wait_timeout(stream: int) -> int:
     """Queue the bounded-wait self-test kernel (see include/fa.h)."""
     return int(load_library().fa_selftest_wait_timeout(stream))
+
+
+def fa_selftest_fwd_fault(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, N: int, D: int, scale: float,
+                          causal: int, dtype: int, fault_item: int, stream: int) -> int:
+    """The forward kernel with one K/V copy left out (test of the give-up path;
+    see include/fa.h)."""
+    return int(load_library().fa_selftest_fwd_fault(q, k, v, o, lse, B, H, N, D, float(scale), int(causal),
+                                                    int(dtype), int(fault_item), stream))
+
+
+def fa_selftest_bwd_fault(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int, B: int,
+                          H: int, N: int, D: int, scale: float, causal: int, dtype: int, workspace: int,
+                          workspace_bytes: int, fault_step: int, stream: int) -> int:
+    """The backward kernels with one Q copy left out (test of the give-up path;
+    see include/fa.h)."""
+    return int(load_library().fa_selftest_bwd_fault(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, D, float(scale),
+                                                    int(causal), int(dtype), workspace, int(workspace_bytes),
+                                                    int(fault_step), stream))
 
 
 def fa_status_string(status: int) -> str:

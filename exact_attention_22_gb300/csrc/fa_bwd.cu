@@ -122,6 +122,10 @@ struct Params {
     int n_tiles;          // BHkv * T
     float scale;
     float scale_log2;     // scale * log2(e)
+    // Test only (fa_selftest_bwd_fault): the loader of every CTA issues no copy
+    // for the Q tile of its step of this index, so the waits on it run out; -1
+    // in every other launch.
+    int fault_step;
 };
 
 // Work tile: K/V tile j of K/V plane kvbh.  Its steps visit Q tiles
@@ -238,11 +242,13 @@ __device__ void run_load(State& st, uint8_t* smem, const CUtensorMap* tm_q, cons
                 ok = false;
                 break;
             }
-            mbar_arrive_expect_tx(&st.q_full[slot], C::kTileBytes);
-            for (int b = 0; b < C::kBoxes; ++b)
-                tma_load_3d_hint(smem + C::kOffQ + slot * C::kTileBytes + b * C::kBoxBytes, tm_q, &st.q_full[slot],
-                                 64 * b, i * kTile, qbh, pol_keep);
-            ++q_loads[slot];
+            if (g != p.fault_step) {   // test only: the fault step's Q copy is never issued
+                mbar_arrive_expect_tx(&st.q_full[slot], C::kTileBytes);
+                for (int b = 0; b < C::kBoxes; ++b)
+                    tma_load_3d_hint(smem + C::kOffQ + slot * C::kTileBytes + b * C::kBoxBytes, tm_q,
+                                     &st.q_full[slot], 64 * b, i * kTile, qbh, pol_keep);
+                ++q_loads[slot];
+            }
             if (!wait_bar(&st.do_empty[slot], ph, abort_flag)) {
                 ok = false;
                 break;
@@ -964,10 +970,13 @@ extern "C" size_t fa_bwd_workspace_bytes(int B, int H, int N, int D) {
            bwd::round256(static_cast<size_t>(rows) * sizeof(float));
 }
 
-extern "C" int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                          const float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int D,
-                          float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
-                          cudaStream_t stream) {
+namespace fa103 {
+namespace bwd {
+
+// fa_bwd_gqa, with the test-only fault step of the loader (-1: none).
+static int entry(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int D, float scale, int causal,
+                 int dtype, void* workspace, size_t workspace_bytes, int fault_step, cudaStream_t stream) {
     if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
     if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
@@ -1019,6 +1028,7 @@ extern "C" int fa_bwd_gqa(const void* q, const void* k, const void* v, const voi
     p.n_tiles = static_cast<int>(T * BHkv);
     p.scale = scale;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.fault_step = fault_step;
     const long long nrows = static_cast<long long>(rows);
     cudaError_t e;
     if (D == 128)
@@ -1028,6 +1038,26 @@ extern "C" int fa_bwd_gqa(const void* q, const void* k, const void* v, const voi
         e = dtype == FA_BF16 ? bwd::launch_all<64, true>(maps, p, causal, o, dout, dq, nrows, stream)
                              : bwd::launch_all<64, false>(maps, p, causal, o, dout, dq, nrows, stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace bwd
+}  // namespace fa103
+
+extern "C" int fa_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv, int N, int D,
+                          float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+    return bwd::entry(q, k, v, o, dout, lse, dq, dk, dv, B, H, H_kv, N, D, scale, causal, dtype, workspace,
+                      workspace_bytes, -1, stream);
+}
+
+extern "C" int fa_selftest_bwd_fault(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int D,
+                                     float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                                     int fault_step, cudaStream_t stream) {
+    if (fault_step < 0) return FA_ERR_INVALID_ARG;
+    return bwd::entry(q, k, v, o, dout, lse, dq, dk, dv, B, H, H, N, D, scale, causal, dtype, workspace,
+                      workspace_bytes, fault_step, stream);
 }
 
 extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,

@@ -134,6 +134,10 @@ struct Params {
     const float* k_scale;
     const float* v_scale;
     int n_blocks;
+    // Test only (fa_selftest_fwd_fault): the K/V producer of every CTA issues
+    // no copy for its ring item of this index, so the waits on it run out; -1
+    // in every other launch.
+    int fault_item;
 };
 
 // One work tile: query rows q0 .. q0+255 of head bh, K/V tiles j0 .. j0+n_all-1
@@ -283,6 +287,7 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
                     ok = false;
                     break;
                 }
+                if (item == p.fault_item) continue;   // test only: this copy is never issued
                 mbar_arrive_expect_tx(&sh.kv_full[slot], C::kTileBytes);
                 const CUtensorMap* map = kind ? tm_v : tm_k;
                 uint8_t* dst = tiles + C::kOffKV + slot * C::kTileBytes;
@@ -303,7 +308,7 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
         // shared memory goes away: the last item of each slot is enough.
         volatile int never = 0;
         for (int last = item - 1; last >= 0 && last >= item - C::kStages; --last)
-            wait_bar(&sh.kv_full[last % C::kStages], (last / C::kStages) & 1, &never);
+            if (last != p.fault_item) wait_bar(&sh.kv_full[last % C::kStages], (last / C::kStages) & 1, &never);
     }
 }
 
@@ -972,14 +977,10 @@ using namespace fa103;
 
 namespace fa103 {
 
-// Argument checks and kernel parameters shared by the 16-bit forward entry
-// points.  Q, O, LSE have Nq rows per head, K and V Nk rows per K/V head.  With
-// `pack`, the query heads that share a K/V head are stacked into one Q plane of
-// (H / H_kv) * Nq rows (their rows are adjacent in memory), so one K/V head is
-// streamed once for all of them.
-static int prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int Nq,
-                   int Nk, int D, float scale, int causal, int dtype, int n_splits, bool pack, CUtensorMap (&maps)[3],
-                   Params& p) {
+// The argument checks of the 16-bit forward entry points, alone (no CUDA call
+// is made): FA_OK or the status the entry point returns.
+static int check_args(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
+                      int Nq, int Nk, int D, float scale, int causal, int dtype, int n_splits, bool pack) {
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_INVALID_ARG;
     if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
@@ -1009,7 +1010,24 @@ static int prepare(const void* q, const void* k, const void* v, void* o, float* 
         if (overlaps(o, tbytes, ins[i], in_bytes[i]) || overlaps(lse, lbytes, ins[i], in_bytes[i]))
             return FA_ERR_INVALID_ARG;
     if (overlaps(o, tbytes, lse, lbytes)) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
 
+// Argument checks and kernel parameters shared by the 16-bit forward entry
+// points.  Q, O, LSE have Nq rows per head, K and V Nk rows per K/V head.  With
+// `pack`, the query heads that share a K/V head are stacked into one Q plane of
+// (H / H_kv) * Nq rows (their rows are adjacent in memory), so one K/V head is
+// streamed once for all of them.
+static int prepare(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv, int Nq,
+                   int Nk, int D, float scale, int causal, int dtype, int n_splits, bool pack, CUtensorMap (&maps)[3],
+                   Params& p) {
+    const int st = check_args(q, k, v, o, lse, B, H, H_kv, Nq, Nk, D, scale, causal, dtype, n_splits, pack);
+    if (st != FA_OK) return st;
+    const uint64_t BH = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
+    const uint64_t BHkv = static_cast<uint64_t>(B) * static_cast<uint64_t>(H_kv);
+    const uint64_t planes = pack ? BHkv : BH;
+    const uint64_t rows = pack ? static_cast<uint64_t>(H / H_kv) * Nq : static_cast<uint64_t>(Nq);
+    const uint64_t n_qblocks = (rows + kRowsPerTile - 1) / kRowsPerTile;
     if (!make_tile_map(&maps[0], q, dtype, D, static_cast<int>(rows), static_cast<int>(planes)) ||
         !make_tile_map(&maps[1], k, dtype, D, Nk, static_cast<int>(BHkv)) ||
         !make_tile_map(&maps[2], v, dtype, D, Nk, static_cast<int>(BHkv)))
@@ -1032,6 +1050,7 @@ static int prepare(const void* q, const void* k, const void* v, void* o, float* 
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.q_scale = p.k_scale = p.v_scale = nullptr;
     p.n_blocks = 0;
+    p.fault_item = -1;
     return FA_OK;
 }
 
@@ -1260,6 +1279,7 @@ extern "C" int fa_fwd_fp8(const void* q, const void* k, const void* v_t, const f
     p.k_scale = k_scale;
     p.v_scale = v_scale;
     p.n_blocks = n_blocks;
+    p.fault_item = -1;
     const cudaError_t e = causal ? launch<128, true, true, false, true>(maps[0], maps[1], maps[2], p, stream)
                                  : launch<128, true, false, false, true>(maps[0], maps[1], maps[2], p, stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -1279,23 +1299,63 @@ constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;   // 64 MiB per device
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device.  In host code the array's name is only a stand-in for the
-// symbol, so the kernels must be given this address, never the name.
+// Id of the current CUDA context, unique within the process (0 if it cannot be
+// read).  A device's context is re-created after cudaDeviceReset, and the
+// library's module, with g_noalloc_scratch, is then loaded again, possibly at
+// another address: the cached address below is valid only for the context it
+// was looked up in.
+static unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up with
+// that device current the first time it is needed in its context and cached
+// per device with the context's id.  In host code the array's name is only a
+// stand-in for the symbol, so the kernels must be given this address, never
+// the name.
 static int noalloc_scratch(void** out) {
-    static std::atomic<void*> cache[64];
+    struct Entry {
+        unsigned long long ctx_id;
+        void* ptr;
+    };
+    static Entry cache[64];
+    static std::mutex mu;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-    if (dev >= 0 && dev < 64) {
-        void* p = cache[dev].load();
-        if (p != nullptr) {
-            *out = p;
+    const bool cached_dev = dev >= 0 && dev < 64;
+    unsigned long long id = current_context_id();
+    if (cached_dev && id != 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cache[dev].ctx_id == id && cache[dev].ptr != nullptr) {
+            *out = cache[dev].ptr;
             return FA_OK;
         }
     }
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return FA_ERR_CUDA;
-    if (dev >= 0 && dev < 64) cache[dev].store(p);
+    id = current_context_id();   // the look-up makes the device's context current if it was not yet
+    if (cached_dev && id != 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache[dev] = Entry{id, p};
+    }
     *out = p;
     return FA_OK;
 }
@@ -1308,13 +1368,28 @@ extern "C" int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* 
                                       int H, int N, int D, float scale, int causal, int dtype, int num_splits,
                                       cudaStream_t stream) {
     if (num_splits < 1 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
-    // Invalid sizes give 0 here and are reported by fa_fwd_splitkv below.
+    // Every argument is checked before the scratch address is looked up (the
+    // first CUDA call), so bad arguments give the same status as fa_fwd_splitkv.
+    const int bad = check_args(q, k, v, o, lse, B, H, H, N, N, D, scale, causal, dtype, num_splits, false);
+    if (bad != FA_OK) return bad;
     if (fa_splitkv_workspace_bytes(B, H, N, D, num_splits) > kNoAllocScratchBytes) return FA_ERR_TOO_LARGE;
     void* scratch = nullptr;
     const int st = noalloc_scratch(&scratch);
     if (st != FA_OK) return st;
     return fa_fwd_splitkv(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, num_splits, scratch,
                           kNoAllocScratchBytes, stream);
+}
+
+extern "C" int fa_selftest_fwd_fault(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                     int N, int D, float scale, int causal, int dtype, int fault_item,
+                                     cudaStream_t stream) {
+    if (fault_item < 0) return FA_ERR_INVALID_ARG;
+    CUtensorMap maps[3];
+    Params p;
+    const int st = prepare(q, k, v, o, lse, B, H, H, N, N, D, scale, causal, dtype, 1, false, maps, p);
+    if (st != FA_OK) return st;
+    p.fault_item = fault_item;
+    return dispatch<false>(maps, p, D, dtype, causal, stream);
 }
 
 extern "C" int fa_selftest_wait_timeout(cudaStream_t stream) {

@@ -139,8 +139,14 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
  *     fa_splitkv_workspace_bytes(B, H, N, D, num_splits) exceeds the scratch
  *     size (use fewer splits, or fa_fwd_splitkv with your own workspace);
  *   - no allocation of any kind is made: the first call on a device looks up
- *     the buffer's device address (once per device, with that device current);
- *     make that first call before any stream capture on that device;
+ *     the buffer's device address (once per device, with that device current)
+ *     and caches it with the id of the device's CUDA context; make that first
+ *     call before any stream capture on that device.  A context re-created
+ *     later (after cudaDeviceReset) may hold the buffer at another address, so
+ *     the first call in the new context looks it up again: that call, too,
+ *     belongs before any stream capture;
+ *   - arguments are checked as fa_fwd_splitkv checks them, before any CUDA
+ *     call is made;
  *   - all calls on a device share the one buffer; calls that may overlap on
  *     the GPU (different streams without ordering between them) race and give
  *     wrong results.  Nothing needs clearing between calls: each call writes
@@ -396,6 +402,38 @@ int fa_get_device_status(cudaStream_t stream);
  * the CUDA context stays usable.  No fault or hang is involved.
  */
 int fa_selftest_wait_timeout(cudaStream_t stream);
+
+/*
+ * fa_selftest_fwd_fault, fa_selftest_bwd_fault -- tests of the give-up path of
+ * the real kernels (the pages have no counterpart; their engineering notes
+ * list a timing violation among the causes of a silent hang, and every wait
+ * here is bounded so that such a fault is reported instead).
+ *
+ * Each takes the arguments of fa_fwd / fa_bwd (same checks, same status
+ * codes) plus a fault index, and launches the same kernels with one load left
+ * out on purpose:
+ *   - fa_selftest_fwd_fault: in every CTA of the forward kernel, the K/V
+ *     producer issues no copy for its ring item `fault_item` (items count
+ *     K_0, V_0, K_1, V_1, ... over the CTA's work tiles; item 2j is K_j of its
+ *     first work tile);
+ *   - fa_selftest_bwd_fault: in every CTA of the backward kernel, the loader
+ *     issues no copy for the Q tile of its step `fault_step` (steps count the
+ *     CTA's Q tiles over its work tiles).
+ * A CTA that reaches that item or step waits for it, gives up after the 1 s
+ * limit, makes its other roles stop, lets its copies and UMMAs in flight
+ * finish, frees its tensor memory and returns; a CTA with fewer items or steps
+ * finishes normally.  fa_get_device_status(stream) then reports
+ * FA_ERR_TIMEOUT and the context stays usable.  The outputs of such a launch
+ * are undefined.  fault_item / fault_step < 0 returns FA_ERR_INVALID_ARG.
+ * No fault, trap or hang of the GPU is involved.
+ */
+int fa_selftest_fwd_fault(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int H, int N, int D, float scale, int causal, int dtype,
+                          int fault_item, cudaStream_t stream);
+int fa_selftest_bwd_fault(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int D,
+                          float scale, int causal, int dtype, void* workspace, size_t workspace_bytes,
+                          int fault_step, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* fa_status_string(int status);

@@ -95,6 +95,32 @@ def test_splitkv_argument_errors_without_gpu(lib, splits, ws, ws_bytes, status):
                              a["causal"], a["dtype"], splits, ws, ws_bytes, 0) == status
 
 
+@pytest.mark.parametrize("kw,splits,status", [
+    (dict(), 0, 1), (dict(), 65, 1),
+    (dict(D=96), 4, 2), (dict(B=0), 4, 1), (dict(N=0), 4, 1), (dict(causal=2), 4, 1), (dict(dtype=2), 4, 1),
+    (dict(scale=0.0), 4, 1), (dict(scale=math.nan), 4, 1),
+    (dict(q=0), 4, 3), (dict(v=(3 << 20) + 2), 4, 3), (dict(lse=(5 << 20) + 4), 4, 3),
+    (dict(o=(1 << 20) + 4096), 4, 1),        # output overlaps q
+])
+def test_noalloc_argument_errors_without_gpu(lib, kw, splits, status):
+    """Every argument is checked before the scratch buffer's address is looked
+    up (without a GPU any CUDA call would give FA_ERR_CUDA instead)."""
+    a = dict(GOOD, **kw)
+    assert fa.fa_fwd_splitkv_noalloc(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"],
+                                     a["scale"], a["causal"], a["dtype"], splits, 0) == status
+
+
+def test_fault_selftests_check_arguments_without_gpu(lib):
+    a = GOOD
+    assert fa.fa_selftest_fwd_fault(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], a["D"],
+                                    a["scale"], a["causal"], a["dtype"], -1, 0) == 1
+    assert fa.fa_selftest_fwd_fault(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"], 96,
+                                    a["scale"], a["causal"], a["dtype"], 3, 0) == 2
+    ptr = [(i + 1) << 20 for i in range(10)]
+    assert fa.fa_selftest_bwd_fault(*ptr[:9], 1, 2, 256, 64, 0.125, 0, 0, ptr[9], 1 << 20, -1, 0) == 1
+    assert fa.fa_selftest_bwd_fault(*ptr[:9], 1, 2, 256, 96, 0.125, 0, 0, ptr[9], 1 << 20, 2, 0) == 2
+
+
 @pytest.mark.parametrize("H,H_kv,status", [(6, 4, 1), (6, 0, 1), (6, -2, 1), (4, 8, 1)])
 def test_gqa_head_count_errors(lib, H, H_kv, status):
     a = GOOD
