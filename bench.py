@@ -20,8 +20,16 @@ Metric: attention forward TFLOP/s with the causal-adjusted FLOP model
   * roofline   tensor-bound: achieved = FLOPs per launch / mean launch time,
                against the measured dense bf16 peak (fp16 has the same
                nominal dense rate, so the ratio is 1).
-  * cpu_baseline  the FP64 CPU oracle, timed on a bounded row sample.
-N > 1 (torchrun): every rank runs the full workload on its own GPU (weak
+  * cpu_baseline  the FP64 CPU oracle timed on the machine's host cores: the
+               plain (naive) form over every row of the workload when that
+               fits about 40 s (else a bounded row sample), the blocked
+               online form on a bounded set of heads, and the naive form on
+               one core.
+  * accuracy   the device result against that naive oracle run: max-abs, RMS
+               and relative L2 error of O, max-abs error of the LSE, and the
+               output type's own rounding floor max|round_t(O_ref) - O_ref|.
+N > 1: one rank per GPU (torchrun; `--gpus N` without torchrun launches the N
+ranks itself).  Every rank runs the full workload on its own GPU (weak
 scaling, no collective on the data path); rank 0 prints the line with the
 slowest rank's time.
 """
@@ -101,6 +109,46 @@ def p95(xs):
     """95th percentile (nearest rank) of the per-step times."""
     ys = sorted(xs)
     return ys[min(len(ys) - 1, max(0, -(-95 * len(ys) // 100) - 1))]
+
+
+def group_median(xs, groups=7):
+    """Median of the means of `groups` consecutive groups of the per-step
+    times (the timing protocol of "CUDA FlashAttention: from online softmax to
+    the long-sequence IO limit", section 8: groups of repetitions, median of
+    the group means).  None with fewer steps than groups."""
+    if len(xs) < groups:
+        return None
+    per = len(xs) // groups
+    return statistics.median(sum(xs[g * per:(g + 1) * per]) / per for g in range(groups))
+
+
+def round_to(x, dtype):
+    """float64 array rounded once, to nearest even, to fp16 or bf16 (values
+    returned as float64)."""
+    import numpy as np
+
+    x = np.asarray(x, dtype=np.float64)
+    if dtype == "fp16":
+        return x.astype(np.float16).astype(np.float64)
+    m, e = np.frexp(x)                      # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)   # 8 significant bits
+
+
+def accuracy_stats(o, lse, o_ref, lse_ref, dtype):
+    """Errors of a device result (O, LSE as float arrays) against the FP64
+    oracle on the same rows: max-abs, RMS and relative L2 of O, max-abs of
+    the LSE, and the floor that rounding the exact O to the output type alone
+    gives, max|round_t(O_ref) - O_ref|."""
+    import numpy as np
+
+    o = np.asarray(o, dtype=np.float64).reshape(o_ref.shape)
+    lse = np.asarray(lse, dtype=np.float64).reshape(lse_ref.shape)
+    d = o - o_ref
+    return {"max_abs_o": float(np.abs(d).max()), "rms_o": float(np.sqrt(np.mean(d * d))),
+            "rel_l2_o": float(np.linalg.norm(d) / max(np.linalg.norm(o_ref), 1e-300)),
+            "max_abs_lse": float(np.abs(lse - lse_ref).max()),
+            "quant_floor_o": float(np.abs(round_to(o_ref, dtype) - o_ref).max()),
+            "elements": int(d.size)}
 
 
 def kernel_source_hash():
@@ -217,6 +265,84 @@ def cpu_oracle_sample(w, seconds=12.0, seed=0, nthreads=0):
     # The FLOP model counts a causal row's half of the full square; the rows'
     # exact visible-key count is used here, which is the same on average.
     return flops / t_total / 1e12, done, t_total, threads, flops
+
+
+def cpu_oracle_blocked(w, seconds=8.0, seed=0, rate_hint=None):
+    """Time the blocked (online-softmax) FP64 oracle, 128 x 128 blocks, on the
+    first min(threads, B*H) heads of the workload, each cut to its first n
+    positions so that the run takes about ``seconds`` (n = N when it fits).
+    Returns (TFLOP/s, heads, n, seconds, threads)."""
+    import numpy as np
+
+    from oracle import fa_ref
+
+    qb, kb, vb = _oracle_inputs(w, seed)
+    threads = fa_ref.max_threads()
+    BH = w.B * w.H
+    heads = min(threads, BH)
+    per_head = 4.0 * w.N * w.N * w.D / (2.0 if w.causal else 1.0)
+    n = w.N
+    if rate_hint:
+        # per-thread rate of the oracle: cut the heads so the run fits
+        budget = rate_hint * 1e12 / threads * seconds
+        if per_head > budget:
+            n = max(256, int(w.N * (budget / per_head) ** 0.5))
+    sl = [np.ascontiguousarray(x.reshape(BH, w.N, w.D)[:heads, :n]).reshape(1, heads, n, w.D) for x in (qb, kb, vb)]
+    t0 = time.perf_counter()
+    fa_ref.blocked(*sl, w.scale, w.causal, Br=128, Bc=128, enc=fa_inputs.enc(w))
+    secs = time.perf_counter() - t0
+    flops = heads * 4.0 * n * n * w.D / (2.0 if w.causal else 1.0)
+    return flops / secs / 1e12, heads, n, secs, threads
+
+
+def cpu_baseline_and_accuracy(w, o, lse, seconds=12.0, seed=0, full_limit=40.0):
+    """The cpu_baseline leg: the naive FP64 oracle on all host cores, over
+    every row of the workload when the estimated time is within
+    ``full_limit`` seconds (else on a bounded random row sample), the blocked
+    oracle beside it, and the naive oracle on one core.  The device result
+    (o, lse: the tensors of the timed run) is compared with the naive run's
+    rows: that comparison is the line's ``accuracy``."""
+    import numpy as np
+
+    from oracle import fa_ref
+
+    est_tf, _, _, threads, _ = cpu_oracle_sample(w, seconds=1.0, seed=seed)
+    full = w.flops / (est_tf * 1e12) <= full_limit
+    o_np = o.float().cpu().numpy()
+    l_np = lse.float().cpu().numpy()
+    if full:
+        qb, kb, vb = _oracle_inputs(w, seed)
+        t0 = time.perf_counter()
+        o_ref, lse_ref = fa_ref.naive(qb, kb, vb, w.scale, w.causal, enc=fa_inputs.enc(w))
+        secs = time.perf_counter() - t0
+        tf, rows = w.flops / secs / 1e12, w.B * w.H * w.N
+        sample = ("every one of the workload's %d query rows, naive FP64 oracle, %.1f s" % (rows, secs))
+        acc = accuracy_stats(o_np, l_np, o_ref, lse_ref, w.dtype)
+        acc["rows"] = "all %d" % rows
+    else:
+        tf, rows, secs, threads, _ = cpu_oracle_sample(w, seconds=seconds, seed=seed)
+        sample = ("%d query rows drawn uniformly at random (with replacement) from the workload's %d rows, "
+                  "naive FP64 oracle, %.1f s" % (rows, w.B * w.H * w.N, secs))
+        rng = np.random.default_rng(4321)
+        bh = rng.integers(0, w.B * w.H, 4096)
+        rr = rng.integers(0, w.N, 4096)
+        qb, kb, vb = _oracle_inputs(w, seed)
+        o_ref, lse_ref = fa_ref.naive_rows(qb, kb, vb, w.scale, w.causal, bh, rr, enc=fa_inputs.enc(w))
+        o_s = o_np.reshape(w.B * w.H, w.N, w.D)[bh, rr]
+        l_s = l_np.reshape(w.B * w.H, w.N)[bh, rr]
+        acc = accuracy_stats(o_s, l_s, o_ref, lse_ref, w.dtype)
+        acc["rows"] = "4096 sampled of %d" % (w.B * w.H * w.N)
+    acc["oracle"] = "naive FP64 (plain safe softmax per row) on the same 16-bit inputs"
+    tf1, rows1, secs1, _, _ = cpu_oracle_sample(w, seconds=3.0, seed=seed, nthreads=1)
+    btf, bheads, bn, bsecs, _ = cpu_oracle_blocked(w, seconds=8.0, seed=seed, rate_hint=tf)
+    base = {
+        "value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
+        "blocked": {"value": btf, "unit": "TFLOP/s", "cores": threads,
+                    "sample": "blocked online-softmax FP64 oracle (128 x 128 blocks) on %d head(s), first %d of "
+                              "%d positions each, %.1f s" % (bheads, bn, w.N, bsecs)},
+        "one_thread": {"value": tf1, "unit": "TFLOP/s", "sample": "%d random rows of the workload, naive FP64 "
+                       "oracle on one core, %.1f s" % (rows1, secs1)}}
+    return base, acc
 
 
 def run_reference(args, w):
@@ -416,6 +542,7 @@ def run_ours(args, w):
                    "scale": w.scale, "parallelism": "replica per GPU" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (256 MiB write, outside the events)",
                    "ms_p50": statistics.median(step_ms), "ms_p95": p95(step_ms), "ms_min": min(step_ms),
+                   "ms_median_of_7_group_means": group_median(step_ms),
                    "num_splits": splits,
                    "entry": "fa_fwd_fp8" if fp8 else ("fa_fwd_splitkv" if splits > 0 else "fa_fwd")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -431,14 +558,8 @@ def run_ours(args, w):
         "kernel_source_sha": kernel_source_hash(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
-        tf, rows, secs, threads, _ = cpu_oracle_sample(w, seconds=args.cpu_seconds)
-        tf1, rows1, secs1, _, _ = cpu_oracle_sample(w, seconds=min(3.0, args.cpu_seconds), nthreads=1)
-        line["cpu_baseline"] = {
-            "value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": ("%d query rows drawn uniformly at random (with replacement) from the workload's %d rows, "
-                       "naive FP64 oracle, %.1f s" % (rows, w.B * w.H * w.N, secs)),
-            "one_thread": {"value": tf1, "unit": "TFLOP/s", "sample": "the first %d rows of the same sample, "
-                           "%.1f s" % (rows1, secs1)}}
+        line["cpu_baseline"], line["accuracy"] = cpu_baseline_and_accuracy(w, o, lse, seconds=args.cpu_seconds,
+                                                                           seed=args.seed)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -563,7 +684,8 @@ def run_ours_bwd(args, w):
         "config": {"workload": w.name, "pass": "bwd", "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
                    "scale": w.scale, "parallelism": "replica per GPU" if world > 1 else "single GPU",
                    "l2": "flushed between timed steps (256 MiB write, outside the events)",
-                   "ms_p50": statistics.median(step_ms), "ms_p95": p95(step_ms), "ms_min": min(step_ms), "entry": "fa_bwd"},
+                   "ms_p50": statistics.median(step_ms), "ms_p95": p95(step_ms), "ms_min": min(step_ms),
+                   "ms_median_of_7_group_means": group_median(step_ms), "entry": "fa_bwd"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None,
                      "peak_kind": "%s dense bf16 (burst); fp16/bf16 nominal ratio 1" % peak_kind,
@@ -684,7 +806,8 @@ def run_decode(args):
         "config": {"workload": args.decode, "B": B, "H": H, "H_kv": H_kv, "Nq": Nq, "Nk": Nk, "D": D,
                    "causal": True, "num_splits": splits, "entry": "fa_fwd_kv",
                    "l2": "flushed between timed steps (256 MiB write, outside the events)",
-                   "ms_p50": statistics.median(step_ms), "ms_p95": p95(step_ms), "ms_min": min(step_ms)},
+                   "ms_p50": statistics.median(step_ms), "ms_p95": p95(step_ms), "ms_min": min(step_ms),
+                   "ms_median_of_7_group_means": group_median(step_ms)},
         "roofline": {"bound": "hbm", "achieved": gbps, "peak": hbm, "unit": "GB/s", "frac": gbps / hbm,
                      "traffic": None, "peak_kind": "%s copy bandwidth" % peak_kind},
         "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
@@ -699,7 +822,39 @@ def run_decode(args):
     return 0
 
 
+def launch_ranks(n, argv):
+    """Run this script as n ranks, one per GPU, through torch.distributed.run
+    on 127.0.0.1 (used when --gpus N > 1 is given without a launcher)."""
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
+def run_dry(args):
+    """The multi-rank plumbing alone, without a GPU: each rank joins a gloo
+    group, the slowest rank's (stand-in) time is taken, and rank 0 prints one
+    line."""
+    import torch.distributed as dist
+
+    world, rank, _ = _dist()
+    if world > 1:
+        dist.init_process_group("gloo")
+    ms = max_over_ranks([1.0 + rank])[0]
+    if rank == 0:
+        print(json.dumps({"dry_run": True, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": ms}), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -718,7 +873,18 @@ def main(argv=None):
                     help="time fa_fwd_fp8 on the workload's shape with E4M3 inputs (D = 128, N a multiple of 16)")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
                     help="time the forward pass (default, the headline) or the backward pass")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="only the rank plumbing (launch, process group, slowest-rank time), no GPU work")
     args = ap.parse_args(argv)
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    world = _dist()[0]
+    if args.gpus != world:
+        if "WORLD_SIZE" in os.environ:
+            ap.error("--gpus %d does not match WORLD_SIZE=%d (one rank per GPU)" % (args.gpus, world))
+        return launch_ranks(args.gpus, argv)
+    if args.dry_run:
+        return run_dry(args)
     args.num_splits_auto = args.num_splits == "auto"
     if args.num_splits_auto and args.decode is None:
         ap.error("--num-splits auto applies to --decode")

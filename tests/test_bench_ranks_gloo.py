@@ -49,3 +49,35 @@ def test_single_process_is_identity():
     import bench
 
     assert bench.max_over_ranks([1.5, 2.5]) == [1.5, 2.5]
+
+
+def _bench(args, env=None):
+    import subprocess
+
+    e = dict(os.environ)
+    for key in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        e.pop(key, None)
+    e.update(env or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, cwd=ROOT, env=e,
+                          capture_output=True, text=True, timeout=300)
+
+
+def test_gpus_flag_launches_that_many_ranks():
+    """`bench.py --gpus 2` without a launcher starts two ranks itself (gloo in
+    this dry run), and rank 0 alone prints the line with n_gpus 2 and the
+    slowest rank's time."""
+    import json
+
+    out = _bench(["--gpus", "2", "--dry-run", "--steps", "3", "--warmup", "3"])
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["ms_per_step"] == 2.0
+
+
+def test_gpus_flag_must_match_the_launcher():
+    out = _bench(["--gpus", "2", "--dry-run"], env={"WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    assert out.returncode != 0 and "WORLD_SIZE" in out.stderr
+    out = _bench(["--gpus", "1", "--dry-run"])
+    assert out.returncode == 0 and '"n_gpus": 1' in out.stdout
