@@ -524,6 +524,21 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
     if (!__all_sync(0xffffffffu, wait_bar(&sh.drain, 0, &never)) && lane_id() == 0) atomicOr(&g_fa_status, ST_DRAIN);
 }
 
+// FP8: the exponent coefficient of K/V tile jg (the Q scale times its K block
+// scale), the log2 shift that folds its V block scale into P (relative to the
+// head's largest, v_ref, times 2^kFp8Shift) and that shift's inverse factor.
+// fold is 2^-shift up to the rounding of the approximate log2 and reciprocal;
+// the row sums are multiplied by fold and O by v_ref / 2^kFp8Shift, so O stays
+// a convex combination of the dequantized V rows with the weights actually used.
+__device__ __forceinline__ void fp8_tile_scales(const Params& p, int kvh, int jg, float c_q, float v_ref,
+                                                float lg_vref, float& c_s, float& shift, float& fold) {
+    const size_t kb = static_cast<size_t>(kvh) * p.n_blocks + jg;
+    const float vs = __ldg(p.v_scale + kb);
+    c_s = c_q * __ldg(p.k_scale + kb);
+    shift = kFp8Shift + (lg2_approx(vs) - lg_vref);
+    fold = v_ref * rcp_approx(vs) * (1.f / kFp8ShiftScale);
+}
+
 template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8>
 __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params& p) {
     static_assert(!(FP8 && SPLIT), "the FP8 path has no split-K form");
@@ -568,8 +583,15 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             v_ref = vm;
         }
         float m_ref = -INFINITY;   // reference max, log2 units of the scaled score
-        float l = 0.f;             // running sum of the 16-bit-rounded P actually used by P V
-        float ls = 0.f;            // running sum of the unrounded p, for the log-sum-exp (bf16)
+        float l = 0.f;             // running sum that normalises O (see the row sums below)
+        float ls = 0.f;            // running sum of the unrounded p, for the log-sum-exp
+        // Coefficient, P shift (log2) and 2^-shift of the next step.  FP8 loads
+        // the next K/V tile's scales one step ahead, off the step's critical path.
+        float c_nx = scale_log2, sh_nx = 0.f, fo_nx = 1.f, lg_vref = 0.f;
+        if constexpr (FP8) {
+            lg_vref = lg2_approx(v_ref);
+            fp8_tile_scales(p, w.kvh, SPLIT ? w.j0 : 0, c_q, v_ref, lg_vref, c_nx, sh_nx, fo_nx);
+        }
         for (int j = 0; j < nkv_t; ++j, ++step) {
             ok = __all_sync(0xffffffffu, wait_bar(&sh.s_full[t], step & 1, abort_flag));
             if (!ok) break;
@@ -579,14 +601,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
 
             const int jg = SPLIT ? w.j0 + j : j;                // global K/V tile index
             const int k0 = jg * kTileN;
-            float c_s = scale_log2, shift = 0.f, fold = 1.f;   // coefficient, P shift (log2), 2^-shift
-            if constexpr (FP8) {
-                const size_t kb = static_cast<size_t>(w.kvh) * p.n_blocks + jg;
-                const float vs = __ldg(p.v_scale + kb);
-                c_s = c_q * __ldg(p.k_scale + kb);
-                shift = kFp8Shift + log2f(vs / v_ref);
-                fold = v_ref / (vs * kFp8ShiftScale);
-            }
+            const float c_s = c_nx, shift = sh_nx, fold = fo_nx;
             // Causal: the row's query is the token at position qpos of the key
             // sequence (qi + Nk - Nq; with stacked heads, its position within its
             // head).  A tile needs the element mask if it holds a key past the
@@ -665,6 +680,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.p_full[t]);
+                if (j + 1 < nkv_t) fp8_tile_scales(p, w.kvh, jg + 1, c_q, v_ref, lg_vref, c_nx, sh_nx, fo_nx);
                 // Row sums of the E4M3 P actually used by P V (normalises O), and of
                 // the unrounded P'' (the log-sum-exp), both back in units of p.
                 float lr[4] = {0.f, 0.f, 0.f, 0.f};
@@ -675,7 +691,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
                 l = l * alpha + ((lr[0] + lr[1]) + (lr[2] + lr[3])) * fold;
                 ls = ls * alpha + (x0 + x1) * fold;
             } else {
-            uint64_t lx2 = pack_f32x2(0.f, 0.f);   // sum of the fp32 p (bf16 only)
+            uint64_t lx2 = pack_f32x2(0.f, 0.f);   // sum of the fp32 p
             uint32_t pk[kTileN / 2];                 // P as packed 16-bit pairs
 #pragma unroll
             for (int i = 0; i < kTileN / 2; ++i) {
@@ -687,6 +703,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
                     lx2 = add_f32x2(lx2, pack_f32x2(p0, p1));
                 } else {
                     pk[i] = pack_f16x2(p0, p1);
+                    lx2 = add_f32x2(lx2, pack_f32x2(p0, p1));
                 }
             }
             tmem_st32(ts, reinterpret_cast<const uint32_t(&)[32]>(pk[0]));
@@ -697,26 +714,26 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             if (lane == 0) mbar_arrive(&sh.p_full[t]);
 
             // The row sums are not needed by the tensor core: they run while it
-            // does this stream's P V and next S.
-            float lr[4] = {0.f, 0.f, 0.f, 0.f};     // sums of the rounded 16-bit P
+            // does this stream's P V and next S.  bf16 normalises O by the sum of
+            // the rounded P that P V actually used (a lone p near 1 rounded to bf16
+            // is off by up to 2^-8, which would bias O by as much); fp16 P is
+            // within 2^-11 of p, so fp16 normalises by the sum of the fp32 p, the
+            // pages' own l, already accumulated in the exponent loop.
+            if constexpr (BF16) {
+                float lr[4] = {0.f, 0.f, 0.f, 0.f};     // sums of the rounded bf16 P
 #pragma unroll
-            for (int i = 0; i < kTileN / 2; ++i) {
-                if constexpr (BF16) {
+                for (int i = 0; i < kTileN / 2; ++i) {
                     lr[i & 3] = add_lo_bf16(pk[i], lr[i & 3]);
                     lr[(i + 2) & 3] = add_hi_bf16(pk[i], lr[(i + 2) & 3]);
-                } else {
-                    lr[i & 3] = add_lo_f16(pk[i], lr[i & 3]);
-                    lr[(i + 2) & 3] = add_hi_f16(pk[i], lr[(i + 2) & 3]);
                 }
-            }
-            l = l * alpha + ((lr[0] + lr[1]) + (lr[2] + lr[3]));
-            if constexpr (BF16) {
+                l = l * alpha + ((lr[0] + lr[1]) + (lr[2] + lr[3]));
                 float x0, x1;
                 unpack_f32x2(lx2, x0, x1);
                 ls = ls * alpha + (x0 + x1);
             } else {
-                // fp16 P is within 2^-11 of p, so the rounded sum also gives the
-                // log-sum-exp to better than 5e-4.
+                float x0, x1;
+                unpack_f32x2(lx2, x0, x1);
+                l = l * alpha + (x0 + x1);
                 ls = l;
             }
             }   // 16-bit P

@@ -412,6 +412,17 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// log2(x) and 1/x for positive normal x, single approximate instructions.
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 // Pack two fp32 values into f16x2 / bf16x2, round to nearest even; `lo` goes
 // to the low 16 bits.
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -485,19 +496,7 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
 }
-// acc + (one 16-bit half of w, widened exactly), in one mixed-precision add.
-__device__ __forceinline__ float add_lo_f16(uint32_t w, float acc) {
-    float r;
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %2;\n\t}"
-        : "=f"(r) : "r"(w), "f"(acc));
-    return r;
-}
-__device__ __forceinline__ float add_hi_f16(uint32_t w, float acc) {
-    float r;
-    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %2;\n\t}"
-        : "=f"(r) : "r"(w), "f"(acc));
-    return r;
-}
+// acc + (one bf16 half of w, widened exactly), in one mixed-precision add.
 __device__ __forceinline__ float add_lo_bf16(uint32_t w, float acc) {
     float r;
     asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
