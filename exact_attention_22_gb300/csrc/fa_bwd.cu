@@ -39,6 +39,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "fa.h"
 #include "fa_host.cuh"
@@ -325,7 +326,6 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
     // as dQ = dS K (M = queries, N = 64): see run_dq.
     constexpr uint32_t kIdQ = D == 128 ? idesc_f16_ab(BF16, kTile, kTile, true, true)
                                        : idesc_f16_ab(BF16, kTile, D, true, true);
-    constexpr int kSteps = D / 16;   // K-steps over the head dimension
     const uint64_t dK = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
     const uint64_t dV = sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
     const uint64_t dKmn = sdesc_sw128(smem_u32(smem + C::kOffK), C::kBoxBytes, 1024);
@@ -338,14 +338,17 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
         dDOk[s] = sdesc_sw128(smem_u32(smem + C::kOffDO + s * C::kTileBytes), 16, 1024);
         dDOmn[s] = sdesc_sw128(smem_u32(smem + C::kOffDO + s * C::kTileBytes), C::kBoxBytes, 1024);
     }
-    // K-major operand, K-step kk over the head dimension: 32 bytes into a
-    // 128-byte row, in box kk / 4 (descriptor units of 16 bytes).
-    auto koff = [](int kk) -> uint64_t {
-        return static_cast<uint64_t>((kk >> 2) * (C::kBoxBytes >> 4) + (kk & 3) * 2);
-    };
     // A operand in TMEM, K-step kk over the 128 queries: P^T / dS^T of queries
     // 0..63 are at columns 0..31, of queries 64..127 at columns 64..95.
-    auto acol = [](int kk) -> uint32_t { return static_cast<uint32_t>(kk < 4 ? 8 * kk : 64 + 8 * (kk - 4)); };
+    using StepsAcol = Steps<0, 8, 16, 24, 64, 72, 80, 88>;
+    using KD = typename std::conditional<D == 128, StepsK8<(C::kBoxBytes >> 4)>, StepsK4>::type;
+    // S^T = K Q^T or dP^T = V dO^T: K-steps over the head dimension, both K-major
+    auto issue_kd = [&](uint32_t d, uint64_t a, uint64_t b) {
+        if constexpr (D == 128)
+            umma_ss_x8<StepOffsets<KD, KD>>(d, a, b, kIdS, 0);
+        else
+            umma_ss_x4<false, StepOffsets<KD, KD>>(d, a, b, kIdS, 0);
+    };
 
     int g = 0;
     bool ok = true;
@@ -369,9 +372,7 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
                     break;
                 }
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kSteps; ++kk)
-                    umma_ss_elect(tmem + C::kTmA, dK + koff(kk), dQk[slot] + koff(kk), kIdS, kk > 0);
+                issue_kd(tmem + C::kTmA, dK, dQk[slot]);
                 umma_commit_elect(&st.s_full);
                 // dP^T into the columns of the previous step's dQ, once that has been read out
                 if (!wait_warp(&st.do_full[slot], ph, abort_flag) ||
@@ -380,9 +381,7 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
                     break;
                 }
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kSteps; ++kk)
-                    umma_ss_elect(tmem + C::kTmB, dV + koff(kk), dDOk[slot] + koff(kk), kIdS, kk > 0);
+                issue_kd(tmem + C::kTmB, dV, dDOk[slot]);
                 umma_commit_elect(&st.dp_full);
                 // dV as soon as P^T is in TMEM, while the compute warps work on dS^T
                 if (!wait_warp(&st.p_ready, g & 1, abort_flag)) {
@@ -395,9 +394,7 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
                     break;
                 }
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kSteps; ++kk)
-                    umma_ss_elect(tmem + C::kTmB, dV + koff(kk), dDOk[slot] + koff(kk), kIdS, kk > 0);
+                issue_kd(tmem + C::kTmB, dV, dDOk[slot]);
                 // S^T into the columns of the previous step's dQ^T, once that has been read out
                 if ((g > 0 && !wait_warp(&st.dq_free, (g - 1) & 1, abort_flag)) ||
                     !wait_warp(&st.q_full[slot], ph, abort_flag)) {
@@ -405,9 +402,7 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
                     break;
                 }
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kSteps; ++kk)
-                    umma_ss_elect(tmem + C::kTmA, dK + koff(kk), dQk[slot] + koff(kk), kIdS, kk > 0);
+                issue_kd(tmem + C::kTmA, dK, dQk[slot]);
                 umma_commit_elect(&st.s_full);   // S^T and dP^T
                 if (!wait_warp(&st.pds_ready, g & 1, abort_flag)) {
                     ok = false;
@@ -416,10 +411,8 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
             }
             tc_fence_after();
             // K-step kk over the queries reads 16 rows = 2048 bytes of dO / Q (MN-major)
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-                umma_ts_elect(tmem + C::kTmDV, tmem + C::kTmA + acol(kk), dDOmn[slot] + 128 * kk, kIdG,
-                              (s > 0 || kk > 0) ? 1u : 0u);
+            umma_ts_x8<StepOffsets<StepsAcol, StepsMN8>>(tmem + C::kTmDV, tmem + C::kTmA, dDOmn[slot], kIdG,
+                                                         s > 0 ? 1u : 0u);
             umma_commit_elect(&st.do_empty[slot]);
             if constexpr (C::kEarlyP) {
                 if (!wait_warp(&st.pds_ready, g & 1, abort_flag)) {
@@ -428,21 +421,16 @@ __device__ void run_mma(State& st, uint8_t* smem, uint32_t tmem, const Params& p
                 }
                 tc_fence_after();
             }
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-                umma_ts_elect(tmem + C::kTmDK, tmem + C::kTmB + acol(kk), dQmn[slot] + 128 * kk, kIdG,
-                              (s > 0 || kk > 0) ? 1u : 0u);
+            umma_ts_x8<StepOffsets<StepsAcol, StepsMN8>>(tmem + C::kTmDK, tmem + C::kTmB, dQmn[slot], kIdG,
+                                                         s > 0 ? 1u : 0u);
             umma_commit_elect(&st.q_empty[slot]);
             // dQ^T = K^T dS^T (D = 128) or dQ = dS K (D = 64), after dK (and dV) have read
             // the TMEM columns it overwrites: K-step kk over the keys reads 16 rows of K
             // and of dS^T in smem, both stored with the M or N index contiguous (MN-major)
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-                if constexpr (D == 128)
-                    umma_ss_elect(tmem + C::kTmDQ, dKmn + 128 * kk, dDSmn + 128 * kk, kIdQ, kk > 0);
-                else
-                    umma_ss_elect(tmem + C::kTmDQ, dDSmn + 128 * kk, dKmn + 128 * kk, kIdQ, kk > 0);
-            }
+            if constexpr (D == 128)
+                umma_ss_x8<StepOffsets<StepsMN8, StepsMN8>>(tmem + C::kTmDQ, dKmn, dDSmn, kIdQ, 0);
+            else
+                umma_ss_x8<StepOffsets<StepsMN8, StepsMN8>>(tmem + C::kTmDQ, dDSmn, dKmn, kIdQ, 0);
             umma_commit_elect(&st.dq_full);
         }
         if (!ok) break;

@@ -398,25 +398,15 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
         const uint64_t da = dq0 + ((t * C::kTileBytes) >> 4);
         const uint64_t db = dkv0 + (((item % C::kStages) * C::kTileBytes) >> 4);
         const uint32_t d = tmem + C::tm_s(t);
+        // K-step kk reads 32 bytes of each 128-byte row of Q and K (16 16-bit or 32
+        // 8-bit elements of D), in box kk / 4
         if constexpr (FP8) {
-            // K-step kk reads 32 columns of D: 32 bytes into the 128-byte row
-            umma_ss_off_elect_f8<0, 0>(d, da, db, kIdS, 0);
-            umma_ss_off_elect_f8<2, 2>(d, da, db, kIdS, 1);
-            umma_ss_off_elect_f8<4, 4>(d, da, db, kIdS, 1);
-            umma_ss_off_elect_f8<6, 6>(d, da, db, kIdS, 1);
+            umma_ss_x4<true, StepOffsets<StepsK4, StepsK4>>(d, da, db, kIdS, 0);
+        } else if constexpr (D == 128) {
+            using K8 = StepsK8<(C::kBoxBytes >> 4)>;
+            umma_ss_x8<StepOffsets<K8, K8>>(d, da, db, kIdS, 0);
         } else {
-        // K-step kk reads 16 columns of D: 32 bytes into a 128-byte row, in box kk / 4
-        umma_ss_off_elect<0, 0>(d, da, db, kIdS, 0);
-        umma_ss_off_elect<2, 2>(d, da, db, kIdS, 1);
-        umma_ss_off_elect<4, 4>(d, da, db, kIdS, 1);
-        umma_ss_off_elect<6, 6>(d, da, db, kIdS, 1);
-        }
-        if constexpr (D == 128 && !FP8) {
-            constexpr uint32_t B = C::kBoxBytes >> 4;
-            umma_ss_off_elect<B + 0, B + 0>(d, da, db, kIdS, 1);
-            umma_ss_off_elect<B + 2, B + 2>(d, da, db, kIdS, 1);
-            umma_ss_off_elect<B + 4, B + 4>(d, da, db, kIdS, 1);
-            umma_ss_off_elect<B + 6, B + 6>(d, da, db, kIdS, 1);
+            umma_ss_x4<false, StepOffsets<StepsK4, StepsK4>>(d, da, db, kIdS, 0);
         }
         umma_commit_elect(&sh.s_full[t]);
         if (release) umma_commit_elect(&sh.kv_empty[item % C::kStages]);
@@ -426,23 +416,11 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
         const uint32_t d = tmem + C::tm_o(t), a = tmem + C::tm_s(t);
         if constexpr (FP8) {
             // K-step kk reads 32 keys: 8 TMEM columns of E4M3 P, 32 bytes of each V^T row
-            umma_ts_off_elect_f8<0>(d, a + 0, dv, kIdO, first ? 0u : 1u);
-            umma_ts_off_elect_f8<2>(d, a + 8, dv, kIdO, 1);
-            umma_ts_off_elect_f8<4>(d, a + 16, dv, kIdO, 1);
-            umma_ts_off_elect_f8<6>(d, a + 24, dv, kIdO, 1);
-            umma_commit_elect(&sh.pv_done[t]);
-            if (release) umma_commit_elect(&sh.kv_empty[item % C::kStages]);
-            return;
+            umma_ts_x4_f8<StepOffsets<StepsCol4, StepsK4>>(d, a, dv, kIdO, first ? 0u : 1u);
+        } else {
+            // K-step kk reads 16 keys = 2048 bytes of V and 8 TMEM columns of P
+            umma_ts_x8<StepOffsets<StepsCol8, StepsMN8>>(d, a, dv, kIdO, first ? 0u : 1u);
         }
-        // K-step kk reads 16 keys = 2048 bytes of V and 8 TMEM columns of P
-        umma_ts_off_elect<0 * 128>(d, a + 0, dv, kIdO, first ? 0u : 1u);
-        umma_ts_off_elect<1 * 128>(d, a + 8, dv, kIdO, 1);
-        umma_ts_off_elect<2 * 128>(d, a + 16, dv, kIdO, 1);
-        umma_ts_off_elect<3 * 128>(d, a + 24, dv, kIdO, 1);
-        umma_ts_off_elect<4 * 128>(d, a + 32, dv, kIdO, 1);
-        umma_ts_off_elect<5 * 128>(d, a + 40, dv, kIdO, 1);
-        umma_ts_off_elect<6 * 128>(d, a + 48, dv, kIdO, 1);
-        umma_ts_off_elect<7 * 128>(d, a + 56, dv, kIdO, 1);
         umma_commit_elect(&sh.pv_done[t]);
         if (release) umma_commit_elect(&sh.kv_empty[item % C::kStages]);
     };

@@ -147,107 +147,10 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit inputs, fp32 accumulate.
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem], A read from tensor memory.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Same two forms with descriptor = base + immediate offset (in 16-byte units),
-// added inside the statement so only the base descriptor stays live.
-template <uint32_t OFF_A, uint32_t OFF_B>
-__device__ __forceinline__ void umma_ss_off(uint32_t d_tmem, uint64_t a_base, uint64_t b_base, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
-        "add.s64 a, %1, %5;\n\t"
-        "add.s64 b, %2, %6;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_A), "n"(OFF_B)
-        : "memory");
-}
-template <uint32_t OFF_B>
-__device__ __forceinline__ void umma_ts_off(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_base, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\t"
-        "add.s64 b, %2, %5;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_B)
-        : "memory");
-}
-// The same two forms and the commit, issued by one lane that elect.sync picks
-// from a converged warp (the lowest active lane, the same one every time for a
-// full warp).  The whole warp runs the issuer's control flow, which then stays
-// warp-uniform: each issue is cheaper than from a lone lane of a divergent
-// branch.
-template <uint32_t OFF_A, uint32_t OFF_B>
-__device__ __forceinline__ void umma_ss_off_elect(uint32_t d_tmem, uint64_t a_base, uint64_t b_base, uint32_t idesc,
-                                                  uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b64 a, b;\n\t"
-        "add.s64 a, %1, %5;\n\t"
-        "add.s64 b, %2, %6;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_A), "n"(OFF_B)
-        : "memory");
-}
-template <uint32_t OFF_B>
-__device__ __forceinline__ void umma_ts_off_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_base, uint32_t idesc,
-                                                  uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b64 b;\n\t"
-        "add.s64 b, %2, %5;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_B)
-        : "memory");
-}
-// kind::f8f6f4 forms (8-bit operands, K = 32 per instruction), elected lane.
-template <uint32_t OFF_A, uint32_t OFF_B>
-__device__ __forceinline__ void umma_ss_off_elect_f8(uint32_t d_tmem, uint64_t a_base, uint64_t b_base, uint32_t idesc,
-                                                     uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b64 a, b;\n\t"
-        "add.s64 a, %1, %5;\n\t"
-        "add.s64 b, %2, %6;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_A), "n"(OFF_B)
-        : "memory");
-}
-template <uint32_t OFF_B>
-__device__ __forceinline__ void umma_ts_off_elect_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_base, uint32_t idesc,
-                                                     uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t.reg .b64 b;\n\t"
-        "add.s64 b, %2, %5;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], b, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(OFF_B)
-        : "memory");
-}
+// Commit issued by the lane elect.sync picks from a converged warp (the lowest
+// active lane, the same one every time for a full warp): arrive once on `bar`
+// when every tcgen05.mma that lane issued before has completed.  The whole
+// issuing warp runs the issuer's control flow, which stays warp-uniform.
 __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -255,13 +158,119 @@ __device__ __forceinline__ void umma_commit_elect(uint64_t* bar) {
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
         : "memory");
 }
-// Arrive once on `bar` when every previously issued tcgen05.mma of this
-// thread has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
+
+// ---------------------------------------------------------------- UMMA groups
+// The K-steps of one operation issued as a group under a single elect.sync.
+// The shared-memory descriptors' start-address fields (16-byte units in the
+// low bits) move by 32-bit adds on their low words, which never carry into the
+// high word for shared-memory addresses; the accumulate predicate is the
+// caller's for the first step and true after it.  Issuing a group costs the
+// issuing warp a handful of instructions per UMMA, and that warp shares its SM
+// sub-partition with warps on the critical path of every step.
+//
+// Step offsets come from a type O: O::a[i] and O::b[i] for step i (a[0] and
+// b[0] are 0: the first step uses the bases as given).  For the TMEM-A forms
+// O::a[i] is a column offset of the A operand.
+template <uint32_t... V>
+struct Steps {
+    static constexpr uint32_t v[sizeof...(V)] = {V...};
+};
+template <class A, class B>
+struct StepOffsets {
+    static constexpr const uint32_t* a = A::v;
+    static constexpr const uint32_t* b = B::v;
+};
+
+#define FA_UMMA_SS_HEAD                                                     \
+    "{\n\t.reg .pred p, e, one;\n\t.reg .b32 al, ah, bl, bh, al2, bl2;\n\t" \
+    ".reg .b64 a, b;\n\t"                                                   \
+    "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"                    \
+    "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 one, 0, 0;\n\t"                  \
+    "elect.sync _|e, 0xffffffff;\n\t"
+#define FA_UMMA_SS_FIRST(kind) "@e tcgen05.mma.cta_group::1." kind " [%0], %1, %2, %3, p;\n\t"
+#define FA_UMMA_SS_NEXT(kind, ia, ib)                                                          \
+    "add.u32 al2, al, %" #ia ";\n\tadd.u32 bl2, bl, %" #ib ";\n\t"                             \
+    "mov.b64 a, {al2, ah};\n\tmov.b64 b, {bl2, bh};\n\t"                                       \
+    "@e tcgen05.mma.cta_group::1." kind " [%0], a, b, %3, one;\n\t"
+#define FA_UMMA_TS_HEAD                                                          \
+    "{\n\t.reg .pred p, e, one;\n\t.reg .b32 bl, bh, bl2;\n\t.reg .b64 b;\n\t" \
+    "mov.b64 {bl, bh}, %2;\n\t"                                                  \
+    "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 one, 0, 0;\n\t"                       \
+    "elect.sync _|e, 0xffffffff;\n\t"
+#define FA_UMMA_TS_FIRST(kind) "@e tcgen05.mma.cta_group::1." kind " [%0], [%1], %2, %3, p;\n\t"
+#define FA_UMMA_TS_NEXT(kind, ia, ib)                                  \
+    "add.u32 bl2, bl, %" #ib ";\n\tmov.b64 b, {bl2, bh};\n\t"          \
+    "@e tcgen05.mma.cta_group::1." kind " [%0], [%1+%" #ia "], b, %3, one;\n\t"
+
+#define FA_UMMA_OPS4(O) "n"(O::a[1]), "n"(O::b[1]), "n"(O::a[2]), "n"(O::b[2]), "n"(O::a[3]), "n"(O::b[3])
+#define FA_UMMA_OPS8(O)                                                                             \
+    FA_UMMA_OPS4(O), "n"(O::a[4]), "n"(O::b[4]), "n"(O::a[5]), "n"(O::b[5]), "n"(O::a[6]), "n"(O::b[6]), \
+        "n"(O::a[7]), "n"(O::b[7])
+
+// Four / eight steps, both operands in shared memory (kind::f8f6f4 when F8).
+template <bool F8, class O>
+__device__ __forceinline__ void umma_ss_x4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    if constexpr (F8)
+        asm volatile(FA_UMMA_SS_HEAD FA_UMMA_SS_FIRST("kind::f8f6f4") FA_UMMA_SS_NEXT("kind::f8f6f4", 5, 6)
+                         FA_UMMA_SS_NEXT("kind::f8f6f4", 7, 8) FA_UMMA_SS_NEXT("kind::f8f6f4", 9, 10) "}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), FA_UMMA_OPS4(O)
+                     : "memory");
+    else
+        asm volatile(FA_UMMA_SS_HEAD FA_UMMA_SS_FIRST("kind::f16") FA_UMMA_SS_NEXT("kind::f16", 5, 6)
+                         FA_UMMA_SS_NEXT("kind::f16", 7, 8) FA_UMMA_SS_NEXT("kind::f16", 9, 10) "}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), FA_UMMA_OPS4(O)
+                     : "memory");
+}
+template <class O>
+__device__ __forceinline__ void umma_ss_x8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(FA_UMMA_SS_HEAD FA_UMMA_SS_FIRST("kind::f16") FA_UMMA_SS_NEXT("kind::f16", 5, 6)
+                     FA_UMMA_SS_NEXT("kind::f16", 7, 8) FA_UMMA_SS_NEXT("kind::f16", 9, 10)
+                         FA_UMMA_SS_NEXT("kind::f16", 11, 12) FA_UMMA_SS_NEXT("kind::f16", 13, 14)
+                             FA_UMMA_SS_NEXT("kind::f16", 15, 16) FA_UMMA_SS_NEXT("kind::f16", 17, 18) "}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), FA_UMMA_OPS8(O)
                  : "memory");
 }
+// Four / eight steps, A in tensor memory (its column offsets in O::a).
+template <class O>
+__device__ __forceinline__ void umma_ts_x4_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(FA_UMMA_TS_HEAD FA_UMMA_TS_FIRST("kind::f8f6f4") FA_UMMA_TS_NEXT("kind::f8f6f4", 5, 6)
+                     FA_UMMA_TS_NEXT("kind::f8f6f4", 7, 8) FA_UMMA_TS_NEXT("kind::f8f6f4", 9, 10) "}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), FA_UMMA_OPS4(O)
+                 : "memory");
+}
+template <class O>
+__device__ __forceinline__ void umma_ts_x8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(FA_UMMA_TS_HEAD FA_UMMA_TS_FIRST("kind::f16") FA_UMMA_TS_NEXT("kind::f16", 5, 6)
+                     FA_UMMA_TS_NEXT("kind::f16", 7, 8) FA_UMMA_TS_NEXT("kind::f16", 9, 10)
+                         FA_UMMA_TS_NEXT("kind::f16", 11, 12) FA_UMMA_TS_NEXT("kind::f16", 13, 14)
+                             FA_UMMA_TS_NEXT("kind::f16", 15, 16) FA_UMMA_TS_NEXT("kind::f16", 17, 18) "}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), FA_UMMA_OPS8(O)
+                 : "memory");
+}
+#undef FA_UMMA_OPS8
+#undef FA_UMMA_OPS4
+#undef FA_UMMA_TS_NEXT
+#undef FA_UMMA_TS_FIRST
+#undef FA_UMMA_TS_HEAD
+#undef FA_UMMA_SS_NEXT
+#undef FA_UMMA_SS_FIRST
+#undef FA_UMMA_SS_HEAD
+
+// Common step patterns (descriptor units of 16 bytes; TMEM columns).
+// K-major operand over a 128-byte-swizzled head dimension: 32 bytes per step
+// (16 16-bit or 32 8-bit elements), the next 128-byte box after four steps.
+using StepsK4 = Steps<0, 2, 4, 6>;
+template <uint32_t kBox>
+using StepsK8 = Steps<0, 2, 4, 6, kBox, kBox + 2, kBox + 4, kBox + 6>;
+// MN-major operand: 16 rows (2048 bytes) per step.
+using StepsMN8 = Steps<0, 128, 256, 384, 512, 640, 768, 896>;
+// 16-bit A operand in TMEM: 16 keys (8 columns of packed pairs) per step.
+using StepsCol8 = Steps<0, 8, 16, 24, 32, 40, 48, 56>;
+using StepsCol4 = Steps<0, 8, 16, 24>;
 
 // Shared-memory matrix descriptor, 128-byte swizzle.  `lbo` / `sbo` are the
 // leading / stride byte offsets of the canonical layout.
@@ -289,28 +298,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
 // The same with A's major-ness too (a_mn_major: A is stored M-contiguous).
 __host__ __device__ constexpr uint32_t idesc_f16_ab(bool bf16, int M, int N, bool a_mn_major, bool b_mn_major) {
     return idesc_f16(bf16, M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
-}
-
-// Runtime-descriptor forms, issued by the lane elect.sync picks.
-__device__ __forceinline__ void umma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void umma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                              uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
 }
 
 // 32 lanes x 32 bit, 32 consecutive columns per thread, without the wait.
