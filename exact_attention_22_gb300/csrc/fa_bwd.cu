@@ -273,7 +273,7 @@ __device__ void run_load(State& st, uint8_t* smem, const CUtensorMap* tm_q, cons
     }
 }
 
-// LSE (converted to log2 units) and Delta of the step's 128 query rows into a
+// -LSE (converted to log2 units) and -Delta of the step's 128 query rows into a
 // shared-memory stage; rows past N get LSE = +inf (so P = 0) and Delta = 0.
 template <int D, bool CAUSAL>
 __device__ void run_stats(State& st, uint8_t* smem, const Params& p) {
@@ -299,8 +299,9 @@ __device__ void run_stats(State& st, uint8_t* smem, const Params& p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const bool in = q + e < p.N;
-                a[e] = in ? p.lse[rowbase + q + e] * kLog2e : INFINITY;
-                b[e] = in ? p.delta[rowbase + q + e] : 0.f;
+                // negated, so the compute warps add them with packed FMA / add
+                a[e] = in ? -(p.lse[rowbase + q + e] * kLog2e) : -INFINITY;
+                b[e] = in ? -p.delta[rowbase + q + e] : 0.f;
             }
             *reinterpret_cast<float4*>(lse2s + stage * kTile + 4 * lane) = make_float4(a[0], a[1], a[2], a[3]);
             *reinterpret_cast<float4*>(dls + stage * kTile + 4 * lane) = make_float4(b[0], b[1], b[2], b[3]);
@@ -465,7 +466,7 @@ __device__ void run_compute(State& st, uint8_t* smem, uint32_t tmem, int wg, con
     const float* dls = lse2s + 2 * kTile;
     const uint32_t ds_row = smem_u32(smem + C::kOffDS + wg * C::kBoxBytes) + static_cast<uint32_t>(r) * 128u;
     const uint32_t sw = static_cast<uint32_t>(r & 7);
-    const float c_log2 = p.scale_log2;
+    const uint64_t c2 = pack_f32x2(p.scale_log2, p.scale_log2);
     int g = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -494,11 +495,15 @@ __device__ void run_compute(State& st, uint8_t* smem, uint32_t tmem, int wg, con
                     uint32_t pp[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const float4 l4 = L[e / 4];
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                        const float4 l4 = L[e / 4];   // -LSE (log2 units)
+                        float x[4];
+                        unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2,
+                                               pack_f32x2(l4.x, l4.y)), x[0], x[1]);
+                        unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), c2,
+                                               pack_f32x2(l4.z, l4.w)), x[2], x[3]);
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
-                            float pr = ex2_approx(fmaf(__uint_as_float(sv[e + h]), c_log2, -lv[h]));
+                            float pr = ex2_approx(x[h]);
                             if (!key_ok || (diag && r > col + e + h)) pr = 0.f;
                             pk[c][e + h] = pr;
                         }
@@ -530,11 +535,16 @@ __device__ void run_compute(State& st, uint8_t* smem, uint32_t tmem, int wg, con
                     uint32_t dd[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const float4 d4 = Dl[e / 4];
-                        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+                        const float4 d4 = Dl[e / 4];   // -Delta
                         float dsv[4];
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) dsv[h] = pk[c][e + h] * (__uint_as_float(dv[e + h]) - dl[h]);
+                        unpack_f32x2(mul_f32x2(pack_f32x2(pk[c][e], pk[c][e + 1]),
+                                               add_f32x2(pack_f32x2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                                         pack_f32x2(d4.x, d4.y))),
+                                     dsv[0], dsv[1]);
+                        unpack_f32x2(mul_f32x2(pack_f32x2(pk[c][e + 2], pk[c][e + 3]),
+                                               add_f32x2(pack_f32x2(__uint_as_float(dv[e + 2]), __uint_as_float(dv[e + 3])),
+                                                         pack_f32x2(d4.z, d4.w))),
+                                     dsv[2], dsv[3]);
                         if constexpr (BF16) {
                             dd[e / 2] = pack_bf16x2(dsv[0], dsv[1]);
                             dd[e / 2 + 1] = pack_bf16x2(dsv[2], dsv[3]);
@@ -566,17 +576,26 @@ __device__ void run_compute(State& st, uint8_t* smem, uint32_t tmem, int wg, con
                     uint32_t pp[16], dd[16];
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const float4 l4 = L[e / 4], d4 = Dl[e / 4];
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-                        float pv[4], dsv[4];
+                        const float4 l4 = L[e / 4], d4 = Dl[e / 4];   // -LSE (log2 units), -Delta
+                        float x[4], pv[4], dsv[4];
+                        unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2,
+                                               pack_f32x2(l4.x, l4.y)), x[0], x[1]);
+                        unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), c2,
+                                               pack_f32x2(l4.z, l4.w)), x[2], x[3]);
 #pragma unroll
                         for (int h = 0; h < 4; ++h) {
-                            float pr = ex2_approx(fmaf(__uint_as_float(sv[e + h]), c_log2, -lv[h]));
+                            float pr = ex2_approx(x[h]);
                             if (!key_ok || (diag && r > col + e + h)) pr = 0.f;
                             pv[h] = pr;
-                            dsv[h] = pr * (__uint_as_float(dv[e + h]) - dl[h]);
                         }
+                        unpack_f32x2(mul_f32x2(pack_f32x2(pv[0], pv[1]),
+                                               add_f32x2(pack_f32x2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                                         pack_f32x2(d4.x, d4.y))),
+                                     dsv[0], dsv[1]);
+                        unpack_f32x2(mul_f32x2(pack_f32x2(pv[2], pv[3]),
+                                               add_f32x2(pack_f32x2(__uint_as_float(dv[e + 2]), __uint_as_float(dv[e + 3])),
+                                                         pack_f32x2(d4.z, d4.w))),
+                                     dsv[2], dsv[3]);
                         if constexpr (BF16) {
                             pp[e / 2] = pack_bf16x2(pv[0], pv[1]);
                             pp[e / 2 + 1] = pack_bf16x2(pv[2], pv[3]);
