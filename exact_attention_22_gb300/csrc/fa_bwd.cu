@@ -23,8 +23,8 @@
 //   * dQ^T = K^T dS^T (TMEM lane = head-dim index) reads dS^T from shared
 //     memory, where the compute warps also write it in the 128-byte-swizzled
 //     layout the tensor core reads.  A dQ warpgroup loads dQ^T from TMEM and
-//     adds scale * dQ^T into the fp32 accumulator with red.global.add, whole
-//     128-byte lines per warp instruction;
+//     adds it (unscaled) into the fp32 accumulator with red.global.add, whole
+//     128-byte lines per warp instruction; the final conversion applies scale;
 //   * K_j and V_j are loaded once per work tile; Q_i and dO_i stream through
 //     two-slot rings; LSE_i (in log2 units) and Delta_i through a two-stage
 //     buffer filled by a loader warp;
@@ -668,7 +668,8 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 }
 
 // dQ warpgroup.  Per step it loads the step's dQ from TMEM, frees TMEM, then
-// adds scale * dQ into the fp32 accumulator with red.global.add.  Measured on
+// adds dS K (not yet multiplied by scale: the conversion kernel does that once)
+// into the fp32 accumulator with red.global.add.  Measured on
 // GB300, each SM's rate of writes into L2 bounds this (plain stores are hardly
 // faster than reductions, and fewer CTAs reducing does not speed up the
 // others), and whole 128-byte lines per warp instruction beat 16-byte pieces
@@ -711,7 +712,6 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
             if (lane == 0) mbar_arrive(&st.dq_free);
             const int q0 = qi * kTile;
             const size_t qplane = static_cast<size_t>(qbh) * p.N;
-            const float sc = p.scale;
             if constexpr (D == 128) {
                 // This thread holds dQ^T for d = 32 quarter + lane and the tile's 128
                 // queries.  Lanes 4m .. 4m+3 transpose each 4 x 4 block (d x query) with
@@ -742,8 +742,7 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
                         const float w0 = b0 ? t1 : mii, w1 = b0 ? mii : t1, w2 = b0 ? t3 : m2i, w3 = b0 ? m2i : t3;
                         const float o0 = b1 ? w2 : w0, o1 = b1 ? w3 : w1, o2 = b1 ? w0 : w2, o3 = b1 ? w1 : w3;
                         const int qc = 32 * part + c0;
-                        if (qc + i < nq)
-                            red_add_v4(base + static_cast<size_t>(qc) * D, o0 * sc, o1 * sc, o2 * sc, o3 * sc);
+                        if (qc + i < nq) red_add_v4(base + static_cast<size_t>(qc) * D, o0, o1, o2, o3);
                     }
                 }
             } else {
@@ -761,7 +760,7 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) a[e][x] = __uint_as_float(v[c][4 * e + x]) * sc;
+                        for (int x = 0; x < 4; ++x) a[e][x] = __uint_as_float(v[c][4 * e + x]);
 #pragma unroll
                     for (int d = 4; d >= 1; d >>= 1) {
                         const bool hi_lane = (lane & d) != 0;
@@ -893,22 +892,24 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const uint16_t* __restr
     if (lane == 0) delta[row] = acc;
 }
 
-// dQ = the fp32 accumulator (already scaled) rounded to 16 bits; one warp per row.
+// dQ = scale * (the fp32 accumulator of dS K) rounded to 16 bits; one warp per row.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq,
-                                                          long long rows) {
+                                                          long long rows, float scale) {
     constexpr int kPer = D / 32;
     const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     const size_t off = static_cast<size_t>(row) * D + lane * kPer;
     if constexpr (kPer == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(dq_acc + off);
+        float4 x = *reinterpret_cast<const float4*>(dq_acc + off);
+        x.x *= scale; x.y *= scale; x.z *= scale; x.w *= scale;
         const uint2 v = BF16 ? make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w))
                              : make_uint2(pack_f16x2(x.x, x.y), pack_f16x2(x.z, x.w));
         *reinterpret_cast<uint2*>(dq + off) = v;
     } else {
-        const float2 x = *reinterpret_cast<const float2*>(dq_acc + off);
+        float2 x = *reinterpret_cast<const float2*>(dq_acc + off);
+        x.x *= scale; x.y *= scale;
         *reinterpret_cast<uint32_t*>(dq + off) = BF16 ? pack_bf16x2(x.x, x.y) : pack_f16x2(x.x, x.y);
     }
 }
@@ -946,7 +947,7 @@ static cudaError_t launch_all(const CUtensorMap (&m)[4], const Params& p, int ca
     if (e != cudaSuccess) return e;
     e = causal ? launch_main<D, BF16, true>(m, p, stream) : launch_main<D, BF16, false>(m, p, stream);
     if (e != cudaSuccess) return e;
-    fa_bwd_post_kernel<D, BF16><<<grid, 256, 0, stream>>>(p.dq_acc, static_cast<uint16_t*>(dq), rows);
+    fa_bwd_post_kernel<D, BF16><<<grid, 256, 0, stream>>>(p.dq_acc, static_cast<uint16_t*>(dq), rows, p.scale);
     return cudaGetLastError();
 }
 
