@@ -662,6 +662,9 @@ __device__ void run_compute(State& st, uint8_t* smem, uint32_t tmem, int wg, con
     if (!ok && lane == 0) give_up(st, ST_COMPUTE);
 }
 
+__device__ __forceinline__ void red_add_v2(float* addr, float a, float b) {
+    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(a), "f"(b) : "memory");
+}
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                  : "memory");
@@ -675,8 +678,8 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
 // others), and whole 128-byte lines per warp instruction beat 16-byte pieces
 // scattered over 32 rows.  So:
 //   D = 128: TMEM holds dQ^T (lane = head-dim index d, column = query); a
-//            4 x 4 transpose among four lanes turns that into 16-byte
-//            reductions, four whole lines (four queries) per warp instruction;
+//            2 x 2 transpose between lane pairs turns that into 8-byte
+//            reductions, two whole lines (two queries) per warp instruction;
 //   D = 64:  TMEM holds dQ (lane = query row, 64 columns); groups of eight
 //            lanes transpose their 8 x 8 blocks of 16-byte pieces, so that a
 //            16-byte reduction instruction covers four whole lines (four
@@ -714,35 +717,25 @@ __device__ void run_dq(State& st, uint32_t tmem, const Params& p) {
             const size_t qplane = static_cast<size_t>(qbh) * p.N;
             if constexpr (D == 128) {
                 // This thread holds dQ^T for d = 32 quarter + lane and the tile's 128
-                // queries.  Lanes 4m .. 4m+3 transpose each 4 x 4 block (d x query) with
-                // two butterfly exchanges, after which lane 4m + i holds d = 32 quarter
-                // + 4m .. 4m+3 of one query and adds them with one 16-byte reduction: a
-                // warp instruction then covers four whole 128-byte lines, not one.
+                // queries.  Lanes 2m and 2m+1 swap one value per pair of queries (a 2 x 2
+                // transpose: one shuffle, three selects), after which lane 2m + b holds
+                // d = 32 quarter + 2m, 2m+1 of query c + b and adds them with one 8-byte
+                // reduction: a warp instruction then covers two whole 128-byte lines.
+                // (A 4 x 4 transpose to 16-byte reductions, four lines per instruction,
+                // costs four shuffles and sixteen selects per reduction and measured 5 %
+                // slower; 4-byte reductions without a transpose, 2 % slower.)
                 const int nq = p.N - q0 < kTile ? p.N - q0 : kTile;
-                const int i = lane & 3;
-                const bool b0 = (i & 1) != 0, b1 = (i & 2) != 0;
-                float* base = p.dq_acc + (qplane + q0 + i) * D + 32 * quarter + 4 * (lane >> 2);
+                const int b = lane & 1;
+                float* base = p.dq_acc + (qplane + q0 + b) * D + 32 * quarter + 2 * (lane >> 1);
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
 #pragma unroll
-                    for (int c0 = 0; c0 < 32; c0 += 4) {
+                    for (int c0 = 0; c0 < 32; c0 += 2) {
                         const float a0 = __uint_as_float(v[part][c0]), a1 = __uint_as_float(v[part][c0 + 1]);
-                        const float a2 = __uint_as_float(v[part][c0 + 2]), a3 = __uint_as_float(v[part][c0 + 3]);
-                        // lane bit 1: keep the query pair (2 b1, 2 b1 + 1), swap the other
-                        const float k0 = b1 ? a2 : a0, k1 = b1 ? a3 : a1;
-                        const float r0 = __shfl_xor_sync(0xffffffffu, b1 ? a0 : a2, 2);
-                        const float r1 = __shfl_xor_sync(0xffffffffu, b1 ? a1 : a3, 2);
-                        // rows (d) i and i^2 of queries i and i^1
-                        const float mii = b0 ? k1 : k0, mij = b0 ? k0 : k1;
-                        const float m2i = b0 ? r1 : r0, m2j = b0 ? r0 : r1;
-                        // lane bit 0: hand query i^1 to lane i^1, get rows i^1 and i^3 of query i
-                        const float t1 = __shfl_xor_sync(0xffffffffu, mij, 1);
-                        const float t3 = __shfl_xor_sync(0xffffffffu, m2j, 1);
-                        // rows i, i^1, i^2, i^3 of query i, put in the order 0 .. 3
-                        const float w0 = b0 ? t1 : mii, w1 = b0 ? mii : t1, w2 = b0 ? t3 : m2i, w3 = b0 ? m2i : t3;
-                        const float o0 = b1 ? w2 : w0, o1 = b1 ? w3 : w1, o2 = b1 ? w0 : w2, o3 = b1 ? w1 : w3;
+                        const float rcv = __shfl_xor_sync(0xffffffffu, b ? a0 : a1, 1);
+                        const float x = b ? rcv : a0, y = b ? a1 : rcv;
                         const int qc = 32 * part + c0;
-                        if (qc + i < nq) red_add_v4(base + static_cast<size_t>(qc) * D, o0, o1, o2, o3);
+                        if (qc + b < nq) red_add_v2(base + static_cast<size_t>(qc) * D, x, y);
                     }
                 }
             } else {
