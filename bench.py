@@ -151,24 +151,26 @@ def accuracy_stats(o, lse, o_ref, lse_ref, dtype):
             "elements": int(d.size)}
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel="fa_fwd.cu"):
+    """Short hash of a kernel's source file and the PTX wrappers it includes."""
     h = hashlib.sha256()
-    for rel in ("exact_attention_22_gb300/csrc/fa_fwd.cu", "exact_attention_22_gb300/csrc/sm103_ptx.cuh"):
+    for rel in ("exact_attention_22_gb300/csrc/" + kernel, "exact_attention_22_gb300/csrc/sm103_ptx.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name):
+def recorded_traffic(key, kernel="fa_fwd.cu"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the kernel source as it is now (else None)."""
+    on the kernel source as it is now (else None).  Backward entries are keyed
+    "bwd:<workload>" and hashed on fa_bwd.cu."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    rec = d.get(workload_name)
-    if not rec or rec.get("kernel_source_sha") != kernel_source_hash():
+    rec = d.get(key)
+    if not rec or rec.get("kernel_source_sha") != kernel_source_hash(kernel):
         return None
     return float(rec["dram_bytes_per_launch"])
 
@@ -687,14 +689,15 @@ def run_ours_bwd(args, w):
                    "ms_p50": statistics.median(step_ms), "ms_p95": p95(step_ms), "ms_min": min(step_ms),
                    "ms_median_of_7_group_means": group_median(step_ms), "entry": "fa_bwd"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": recorded_traffic("bwd:" + w.name, "fa_bwd.cu"),
+                     "traffic_kernel": "fa_bwd_kernel (main kernel of the three)",
                      "peak_kind": "%s dense bf16 (burst); fp16/bf16 nominal ratio 1" % peak_kind,
                      "peak_sustained": sustained, "frac_sustained": achieved / sustained if sustained else None},
         "e2e": {"value": job_tflops(world, flops, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "api": "fa_bwd_host"},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
-        "kernel_source_sha": kernel_source_hash(),
+        "kernel_source_sha": kernel_source_hash("fa_bwd.cu"),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import fa_ref
