@@ -30,7 +30,10 @@
 //   * a correction warpgroup rescales O_t in TMEM when a row's reference max
 //     moves by more than 2^8 (the reference may lag the true max: the
 //     invariant O = sum e^(s - m_ref) v, l = sum e^(s - m_ref) holds for any
-//     m_ref used consistently, so the result is unchanged).
+//     m_ref used consistently, so the result is unchanged);
+//   * with no more work tiles than SMs, a work tile is one 128-row Q tile whose
+//     K/V tiles the two streams share out (key split), their partial (m, l, O)
+//     merged on chip at the end of the tile.
 // Every mbarrier wait is bounded in time; a wait that gives up records a
 // status bit, makes the other roles stop, drains in-flight copies and MMAs,
 // frees TMEM and returns.
@@ -105,8 +108,10 @@ struct __align__(8) SharedState {
     uint64_t p_full[kNumQ];        // softmax + correction -> MMA: P_t in TMEM and O_t rescaled
     uint64_t alpha_ready[kNumQ];   // softmax -> correction: per-row rescale factors published
     uint64_t pv_done[kNumQ];       // MMA -> softmax/correction: O_t += P_t V_j complete
+    uint64_t k_sync[4];            // key split: both streams' warps of one TMEM lane quarter
     uint64_t drain;
     float alpha[kNumQ][kTileM];
+    float4 k_part[kNumQ][kTileM];  // key split: each stream's (m_ref, l, ls) of a row
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -147,8 +152,34 @@ struct Tile {
     int nkv[kNumQ];      // K/V tiles of this chunk each stream visits (0: none)
 };
 
-template <bool CAUSAL, bool SPLIT>
+// Key-split work tiles (KS, few work tiles for the SMs): one 128-row Q tile of
+// one plane; both streams take its rows, stream 0 the first ceil(J/2) of its J
+// K/V tiles and stream 1 the rest (starting at tile j0), and the two partial
+// (m, l, O) are merged at the end of the tile.
+template <bool CAUSAL>
+__device__ __forceinline__ Tile make_tile_ks(const Params& p, int idx) {
+    Tile w;
+    w.split = 0;
+    w.q0 = (p.n_qblocks - 1 - idx / p.BH) * kTileM;   // heaviest first
+    w.bh = idx % p.BH;
+    w.kvh = p.kv_group == 1 ? w.bh : (w.bh / p.H) * (p.H / p.kv_group) + (w.bh % p.H) / p.kv_group;
+    int J;
+    if (CAUSAL) {
+        const int qlast = min(w.q0 + kTileM - 1, p.N - 1);
+        J = qlast + p.causal_off < 0 ? 0 : min(qlast + p.causal_off, p.Nk - 1) / kTileN + 1;
+    } else {
+        J = (p.Nk + kTileN - 1) / kTileN;
+    }
+    w.nkv[0] = (J + 1) / 2;
+    w.nkv[1] = J / 2;
+    w.j0 = w.nkv[0];
+    w.n_all = w.nkv[0];
+    return w;
+}
+
+template <bool CAUSAL, bool SPLIT, bool KS = false>
 __device__ __forceinline__ Tile make_tile(const Params& p, int idx) {
+    if constexpr (KS) return make_tile_ks<CAUSAL>(p, idx);
     Tile w;
     // heaviest query block first: causal work grows with the block index
     const int qbh = SPLIT ? idx / p.n_splits : idx;
@@ -183,6 +214,12 @@ __device__ __forceinline__ Tile make_tile(const Params& p, int idx) {
     }
     return w;
 }
+
+// First query row of stream t's Q tile, and its first K/V tile.
+template <bool KS>
+__device__ __forceinline__ int stream_row0(const Tile& w, int t) { return KS ? w.q0 : w.q0 + kTileM * t; }
+template <bool KS>
+__device__ __forceinline__ int stream_kv0(const Tile& w, int t) { return KS ? (t ? w.j0 : 0) : w.j0; }
 
 // The k-th work tile of this CTA, or -1: rounds of gridDim.x tiles, dealt in a
 // snake order so a CTA that got a heavy tile in one round gets a light one in
@@ -264,7 +301,7 @@ __device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, float (&s)[128])
 // ------------------------------------------------------------------ roles
 
 // K/V producer: one thread; K_j then V_j of every work tile, in order.
-template <int D, bool CAUSAL, bool SPLIT, bool FP8>
+template <int D, bool CAUSAL, bool SPLIT, bool FP8, bool KS>
 __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                 const Params& p) {
     using C = Cfg<D, FP8>;
@@ -277,8 +314,13 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
     for (int k = 0; ok; ++k) {
         const int idx = tile_index(k, p.n_tiles);
         if (idx < 0) break;
-        const Tile w = make_tile<CAUSAL, SPLIT>(p, idx);
-        for (int j = 0; j < w.n_all && ok; ++j) {
+        const Tile w = make_tile<CAUSAL, SPLIT, KS>(p, idx);
+        for (int j = 0; j < w.n_all && ok; ++j)
+#pragma unroll 1
+        for (int t = 0; t < (KS ? kNumQ : 1) && ok; ++t) {
+            // key split: stream 0's j-th K/V tile, then stream 1's (if it has one)
+            if (KS && j >= w.nkv[t]) continue;
+            const int jt = stream_kv0<KS>(w, t) + j;
 #pragma unroll 1
             for (int kind = 0; kind < 2; ++kind, ++item) {   // K_j, then V_j
                 const int slot = item % C::kStages;
@@ -294,11 +336,11 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
                 if (FP8 && kind) {
                     // V is stored transposed per head ([D][N], keys contiguous): one
                     // 128-key x 128-row box, the operand K-major for the FP8 P V
-                    tma_load_3d_hint(dst, map, &sh.kv_full[slot], (w.j0 + j) * kTileN, 0, w.kvh, pol_keep);
+                    tma_load_3d_hint(dst, map, &sh.kv_full[slot], jt * kTileN, 0, w.kvh, pol_keep);
                 } else {
                     for (int b = 0; b < C::kBoxes; ++b)
                         tma_load_3d_hint(dst + b * C::kBoxBytes, map, &sh.kv_full[slot], C::kBoxElems * b,
-                                         (w.j0 + j) * kTileN, w.kvh, pol_keep);
+                                         jt * kTileN, w.kvh, pol_keep);
                 }
             }
         }
@@ -313,7 +355,7 @@ __device__ void run_kv_producer(SharedState& sh, uint8_t* tiles, const CUtensorM
 }
 
 // Q producer: one thread; Q_t of every work tile once its buffer is free.
-template <int D, bool CAUSAL, bool SPLIT, bool FP8>
+template <int D, bool CAUSAL, bool SPLIT, bool FP8, bool KS>
 __device__ void run_q_producer(SharedState& sh, uint8_t* tiles, const CUtensorMap* tm_q, const Params& p) {
     using C = Cfg<D, FP8>;
     volatile int* abort_flag = &sh.abort_flag;
@@ -324,7 +366,7 @@ __device__ void run_q_producer(SharedState& sh, uint8_t* tiles, const CUtensorMa
     for (int k = 0; ok; ++k) {
         const int idx = tile_index(k, p.n_tiles);
         if (idx < 0) break;
-        const Tile w = make_tile<CAUSAL, SPLIT>(p, idx);
+        const Tile w = make_tile<CAUSAL, SPLIT, KS>(p, idx);
         for (int t = 0; t < kNumQ; ++t) {
             if (w.nkv[t] == 0) continue;
             if (!wait_bar(&sh.q_empty[t], (loads[t] & 1) ^ 1, abort_flag)) {
@@ -335,7 +377,7 @@ __device__ void run_q_producer(SharedState& sh, uint8_t* tiles, const CUtensorMa
             mbar_arrive_expect_tx(&sh.q_full[t], C::kTileBytes);
             for (int b = 0; b < C::kBoxes; ++b)
                 tma_load_3d_hint(tiles + C::kOffQ + t * C::kTileBytes + b * C::kBoxBytes, tm_q, &sh.q_full[t],
-                                 C::kBoxElems * b, w.q0 + kTileM * t, w.bh, pol_once);
+                                 C::kBoxElems * b, stream_row0<KS>(w, t), w.bh, pol_once);
             ++loads[t];
         }
     }
@@ -364,7 +406,7 @@ __device__ __forceinline__ uint32_t mbar_test3_bcast(uint64_t* b0, uint32_t p0, 
 // work tile's K_0: a stream's first S of the next tile goes out early, at the
 // end of its previous tile, and stream 0 may start only at the top of the tile
 // (when it had no K/V tiles in the previous one), after stream 1.
-template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8, bool KS>
 __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Params& p) {
     using C = Cfg<D, FP8>;
     volatile int* abort_flag = &sh.abort_flag;
@@ -426,11 +468,14 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
     };
     // First S of stream t in work tile w (ring items from `base`); it releases
     // K_0 unless the other stream reads it and has not issued its first S yet.
+    // (Key split: each stream reads its own K/V tiles, ring items 2 (2 j + t) and
+    // 2 (2 j + t) + 1 of a work tile, each read once.)
     auto start_stream = [&](int t, const Tile& w, int base, bool other_done) -> bool {
         if (!__all_sync(0xffffffffu, wait_bar(&sh.q_full[t], (q_par >> t) & 1, abort_flag))) return false;
         q_par ^= 1u << t;
-        if (!acquire(base)) return false;
-        issue_s(t, base, w.nkv[kNumQ - 1 - t] == 0 || other_done);
+        const int item = KS ? base + 2 * t : base;
+        if (!acquire(item)) return false;
+        issue_s(t, item, KS || w.nkv[kNumQ - 1 - t] == 0 || other_done);
         if (w.nkv[t] == 1) umma_commit_elect(&sh.q_empty[t]);   // that was its last S of this work tile
         return true;
     };
@@ -438,14 +483,14 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
     int k = 0;
     int idx = tile_index(0, p.n_tiles);
     if (idx < 0) return;
-    Tile cur = make_tile<CAUSAL, SPLIT>(p, idx);
+    Tile cur = make_tile<CAUSAL, SPLIT, KS>(p, idx);
     int cur_base = 0;
     uint32_t started = 0;    // bit t: first S of `cur` already issued by the previous tile
     while (ok) {
         const int nidx = tile_index(k + 1, p.n_tiles);
         const bool has_next = nidx >= 0;
-        const Tile nxt = has_next ? make_tile<CAUSAL, SPLIT>(p, nidx) : cur;
-        const int nxt_base = cur_base + 2 * cur.n_all;
+        const Tile nxt = has_next ? make_tile<CAUSAL, SPLIT, KS>(p, nidx) : cur;
+        const int nxt_base = cur_base + (KS ? 2 * (cur.nkv[0] + cur.nkv[1]) : 2 * cur.n_all);
         if (ok && cur.nkv[0] > 0 && !(started & 1u)) {
             ok = start_stream(0, cur, cur_base, (started & 2u) != 0);
             started |= 1u;
@@ -456,13 +501,14 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
 #pragma unroll
             for (int t = 0; t < kNumQ; ++t) {
                 if (!ok || j >= cur.nkv[t]) continue;
-                const int item_v = cur_base + 2 * j + 1;
+                const int item_v = KS ? cur_base + 2 * (2 * j + t) + 1 : cur_base + 2 * j + 1;
                 const bool more = j + 1 < cur.nkv[t];
                 // V_j, K_{j+1} (long since landed) and P_t: the three barriers
                 // are tested together so their latencies overlap; only a test
                 // that fails falls back to a bounded wait.
-                const int need = more ? item_v + 1 : item_v;
-                const int item_k = more ? item_v + 1 : item_v;
+                const int next_k = KS ? cur_base + 2 * (2 * (j + 1) + t) : item_v + 1;
+                const int need = more ? next_k : item_v;
+                const int item_k = more ? next_k : item_v;
                 const uint32_t got = mbar_test3_bcast(&sh.kv_full[item_v % C::kStages], (item_v / C::kStages) & 1,
                                                       &sh.kv_full[item_k % C::kStages], (item_k / C::kStages) & 1,
                                                       &sh.p_full[t], (pv_par >> t) & 1);
@@ -478,10 +524,9 @@ __device__ void run_mma(SharedState& sh, uint8_t* tiles, uint32_t tmem, const Pa
                 }
                 tc_fence_after();
                 pv_par ^= 1u << t;
-                issue_pv(t, item_v, j == 0, t == kNumQ - 1 || j >= cur.nkv[kNumQ - 1]);
+                issue_pv(t, item_v, j == 0, KS || t == kNumQ - 1 || j >= cur.nkv[kNumQ - 1]);
                 if (more) {
-                    const int item_k = item_v + 1;
-                    issue_s(t, item_k, t == kNumQ - 1 || j + 1 >= cur.nkv[kNumQ - 1]);
+                    issue_s(t, next_k, KS || t == kNumQ - 1 || j + 1 >= cur.nkv[kNumQ - 1]);
                     if (j + 2 == cur.nkv[t]) umma_commit_elect(&sh.q_empty[t]);
                 } else if (has_next && nxt.nkv[t] > 0) {
                     ok = start_stream(t, nxt, nxt_base, ((nstarted >> (kNumQ - 1 - t)) & 1u) != 0);
@@ -517,9 +562,10 @@ __device__ __forceinline__ void fp8_tile_scales(const Params& p, int kvh, int jg
     fold = v_ref * rcp_approx(vs) * (1.f / kFp8ShiftScale);
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8, bool KS>
 __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params& p) {
     static_assert(!(FP8 && SPLIT), "the FP8 path has no split-K form");
+    static_assert(!(KS && (FP8 || SPLIT)), "the key split is a 16-bit, single-pass form");
     constexpr float kLazy = FP8 ? kLazyRescaleFp8 : kLazyRescale;
     volatile int* abort_flag = &sh.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -530,16 +576,17 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
     const float scale_log2 = p.scale_log2;
     const int N = p.N;
     int step = 0;   // S/P steps of this stream so far (phase of s_full / p_full / alpha_ready / pv_done)
+    int kph = 0;    // key split: exchanges with the other stream so far (phase of k_sync)
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
         const int idx = tile_index(k, p.n_tiles);
         if (idx < 0) break;
-        const Tile w = make_tile<CAUSAL, SPLIT>(p, idx);
+        const Tile w = make_tile<CAUSAL, SPLIT, KS>(p, idx);
         const int nkv_t = w.nkv[t];
-        const int qi = w.q0 + kTileM * t + r;                 // row of this thread in its Q plane
+        const int qi = stream_row0<KS>(w, t) + r;             // row of this thread in its Q plane
         const size_t row_g = static_cast<size_t>(w.bh) * N + qi;
-        if (nkv_t == 0) {
+        if (!KS && nkv_t == 0) {
             // split mode: this chunk holds none of the stream's keys
             if (SPLIT && qi < N)
                 p.ws_st[static_cast<size_t>(w.split) * p.BH * N + row_g] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
@@ -577,7 +624,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             float s[kTileN];
             tmem_ld128_wait(ts, s);
 
-            const int jg = SPLIT ? w.j0 + j : j;                // global K/V tile index
+            const int jg = (SPLIT || KS) ? stream_kv0<KS>(w, t) + j : j;   // global K/V tile index
             const int k0 = jg * kTileN;
             const float c_s = c_nx, shift = sh_nx, fold = fo_nx;
             // Causal: the row's query is the token at position qpos of the key
@@ -585,7 +632,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
             // head).  A tile needs the element mask if it holds a key past the
             // smallest position of the stream's rows, or keys past Nk.  (Read from
             // the kernel parameters here, not kept live across the loop.)
-            const bool need_mask = (CAUSAL && k0 + kTileN - 1 > (p.packed ? 0 : w.q0 + kTileM * t) + p.causal_off) ||
+            const bool need_mask = (CAUSAL && k0 + kTileN - 1 > (p.packed ? 0 : stream_row0<KS>(w, t)) + p.causal_off) ||
                                    (k0 + kTileN > p.Nk);
             if (need_mask) {
                 const int qpos = (p.packed ? qi % p.q_per : qi) + p.causal_off;
@@ -718,6 +765,75 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
         }
         if (!ok) break;
 
+        if constexpr (KS) {
+            // Key split: merge the two streams' partials of these rows.  Each
+            // stream publishes (m_ref, l, ls) once its last P V is complete; then
+            // each combines its half of the O columns from both O_0 and O_1:
+            //   m = max(m_0, m_1), a_s = 2^(m_s - m), O = sum_s a_s O_s / sum_s a_s l_s.
+            const int quarter = warp & 3;
+            auto exchange = [&]() -> bool {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.k_sync[quarter]);
+                const bool got = __all_sync(0xffffffffu, wait_bar(&sh.k_sync[quarter], kph & 1, abort_flag));
+                ++kph;
+                tc_fence_after();
+                return got;
+            };
+            if (nkv_t > 0) {
+                ok = __all_sync(0xffffffffu, wait_bar(&sh.pv_done[t], (step - 1) & 1, abort_flag));
+                if (!ok) break;
+            }
+            sh.k_part[t][r] = make_float4(m_ref, l, ls, 0.f);
+            if (!exchange()) {
+                ok = false;
+                break;
+            }
+            const float4 other = sh.k_part[t ^ 1][r];
+            const float mm = fmaxf(m_ref, other.x);
+            const float a_me = m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - mm);
+            const float a_ot = other.x == -INFINITY ? 0.f : ex2_approx(other.x - mm);
+            const float lt = a_me * l + a_ot * other.y, lst = a_me * ls + a_ot * other.z;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const bool row_ok = qi < N;
+            constexpr int kHalf = D / 2;   // O columns this stream writes
+            const uint32_t o_me = tmem + lane_addr + Cfg<D>::tm_o(t) + kHalf * t;
+            const uint32_t o_ot = tmem + lane_addr + Cfg<D>::tm_o(t ^ 1) + kHalf * t;
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + (row_ok ? row_g : 0) * D + kHalf * t);
+#pragma unroll
+            for (int c = 0; c < kHalf; c += 32) {
+                uint32_t va[32], vb[32];
+                tmem_ld32_wait(o_me + c, va);
+                tmem_ld32_wait(o_ot + c, vb);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float x[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        // a stream without keys left its O unwritten: its term is 0, not 0 * O
+                        const float pa = a_me != 0.f ? a_me * __uint_as_float(va[2 * i + h]) : 0.f;
+                        const float pb = a_ot != 0.f ? a_ot * __uint_as_float(vb[2 * i + h]) : 0.f;
+                        x[h] = (pa + pb) * inv;
+                    }
+                    pk[i] = BF16 ? pack_bf16x2(x[0], x[1]) : pack_f16x2(x[0], x[1]);
+                }
+                if (row_ok) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        orow[c / 8 + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            if (row_ok && t == 0) p.lse[row_g] = lst > 0.f ? (mm + log2f(lst)) * 0.69314718055994531f : -INFINITY;
+            // Both streams have read O_0 and O_1 before either's next P V overwrites them.
+            if (!exchange()) {
+                ok = false;
+                break;
+            }
+            tc_fence_before();
+            continue;
+        }
+
         // Epilogue of this work tile: wait for the last P V, then O / l -> 16-bit
         // -> global (rows past N are not written) and the LSE.
         ok = __all_sync(0xffffffffu, wait_bar(&sh.pv_done[t], (step - 1) & 1, abort_flag));
@@ -772,7 +888,7 @@ __device__ void run_softmax(SharedState& sh, uint32_t tmem, int t, const Params&
     if (!ok) give_up(sh, ST_SOFTMAX);
 }
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool KS>
 __device__ void run_correction(SharedState& sh, uint32_t tmem, const Params& p) {
     using C = Cfg<D>;
     volatile int* abort_flag = &sh.abort_flag;
@@ -784,7 +900,7 @@ __device__ void run_correction(SharedState& sh, uint32_t tmem, const Params& p) 
     for (int k = 0; ok; ++k) {
         const int idx = tile_index(k, p.n_tiles);
         if (idx < 0) break;
-        const Tile w = make_tile<CAUSAL, SPLIT>(p, idx);
+        const Tile w = make_tile<CAUSAL, SPLIT, KS>(p, idx);
         for (int j = 0; j < w.n_all && ok; ++j) {
             for (int t = 0; t < kNumQ; ++t) {
                 if (j >= w.nkv[t]) continue;
@@ -819,7 +935,7 @@ __device__ void run_correction(SharedState& sh, uint32_t tmem, const Params& p) 
     if (!ok) give_up(sh, ST_CORRECTION);
 }
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8 = false>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8 = false, bool KS = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -838,6 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.alpha_ready[t], 4);
             mbar_init(&sh.pv_done[t], 1);
         }
+        for (int q = 0; q < 4; ++q) mbar_init(&sh.k_sync[q], kNumQ);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&sh.kv_full[s], 1);
             mbar_init(&sh.kv_empty[s], 1);
@@ -858,18 +975,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (wg == 0) {
         setmaxnreg_dec<96>();
         if (warp == 0 && lane == 0)
-            run_kv_producer<D, CAUSAL, SPLIT, FP8>(sh, tiles, &tm_k, &tm_v, p);
+            run_kv_producer<D, CAUSAL, SPLIT, FP8, KS>(sh, tiles, &tm_k, &tm_v, p);
         else if (warp == 1)
-            run_mma<D, BF16, CAUSAL, SPLIT, FP8>(sh, tiles, tmem, p);
+            run_mma<D, BF16, CAUSAL, SPLIT, FP8, KS>(sh, tiles, tmem, p);
         else if (warp == 2 && lane == 0)
-            run_q_producer<D, CAUSAL, SPLIT, FP8>(sh, tiles, &tm_q, p);
+            run_q_producer<D, CAUSAL, SPLIT, FP8, KS>(sh, tiles, &tm_q, p);
         __syncwarp();
     } else if (wg <= kNumQ) {
         setmaxnreg_inc<176>();
-        run_softmax<D, BF16, CAUSAL, SPLIT, FP8>(sh, tmem, wg - 1, p);
+        run_softmax<D, BF16, CAUSAL, SPLIT, FP8, KS>(sh, tmem, wg - 1, p);
     } else {
         setmaxnreg_dec<64>();
-        run_correction<D, CAUSAL, SPLIT>(sh, tmem, p);
+        run_correction<D, CAUSAL, SPLIT, KS>(sh, tmem, p);
     }
 
     tc_fence_before();
@@ -945,10 +1062,10 @@ __global__ void __launch_bounds__(32) selftest_wait_timeout_kernel() {
 
 // ------------------------------------------------------------------ host
 
-template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8 = false>
+template <int D, bool BF16, bool CAUSAL, bool SPLIT, bool FP8 = false, bool KS = false>
 static cudaError_t launch(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
                           cudaStream_t stream) {
-    auto kern = fa_fwd_kernel<D, BF16, CAUSAL, SPLIT, FP8>;
+    auto kern = fa_fwd_kernel<D, BF16, CAUSAL, SPLIT, FP8, KS>;
     static std::atomic<uint64_t> configured{0};   // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1049,11 +1166,12 @@ static int prepare(const void* q, const void* k, const void* v, void* o, float* 
     return FA_OK;
 }
 
-template <bool SPLIT>
-static int dispatch(const CUtensorMap (&m)[3], const Params& p, int D, int dtype, int causal, cudaStream_t stream) {
+template <bool SPLIT, bool KS>
+static int dispatch_as(const CUtensorMap (&m)[3], const Params& p, int D, int dtype, int causal,
+                       cudaStream_t stream) {
     cudaError_t e;
     const bool bf = dtype == FA_BF16;
-#define FA_LAUNCH(DD, BB, CC) e = launch<DD, BB, CC, SPLIT>(m[0], m[1], m[2], p, stream)
+#define FA_LAUNCH(DD, BB, CC) e = launch<DD, BB, CC, SPLIT, false, KS>(m[0], m[1], m[2], p, stream)
     if (D == 64) {
         if (bf) { if (causal) FA_LAUNCH(64, true, true); else FA_LAUNCH(64, true, false); }
         else    { if (causal) FA_LAUNCH(64, false, true); else FA_LAUNCH(64, false, false); }
@@ -1063,6 +1181,32 @@ static int dispatch(const CUtensorMap (&m)[3], const Params& p, int D, int dtype
     }
 #undef FA_LAUNCH
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// The 16-bit forward launch.  With no more 256-row work tiles than SMs (short
+// sequences, few heads), a CTA would run one tile's chains back to back with
+// SMs left idle; the key split then deals 128-row Q tiles instead, each with
+// its K/V tiles shared out between the CTA's two streams (half the chain) and
+// merged on chip.  The choice is made on `ks_tiles` 256-row work tiles (< 0:
+// this launch's).
+template <bool SPLIT>
+static int dispatch(const CUtensorMap (&m)[3], const Params& p, int D, int dtype, int causal, cudaStream_t stream,
+                    long long ks_tiles = -1) {
+    if constexpr (!SPLIT) {
+        if (!p.packed) {
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+            const int sms = sm_count(dev);
+            const long long tiles = ks_tiles < 0 ? p.n_tiles : ks_tiles;
+            if (sms > 0 && tiles <= sms) {
+                Params pk = p;
+                pk.n_qblocks = (p.N + kTileM - 1) / kTileM;
+                pk.n_tiles = pk.n_qblocks * p.BH;
+                return dispatch_as<false, true>(m, pk, D, dtype, causal, stream);
+            }
+        }
+    }
+    return dispatch_as<SPLIT, false>(m, p, D, dtype, causal, stream);
 }
 
 static int dispatch_merge(const Params& p, int D, int dtype, cudaStream_t stream) {
@@ -1095,6 +1239,20 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
     if (st != FA_OK) return st;
     return dispatch<false>(maps, p, D, dtype, causal, stream);
 }
+
+namespace fa103 {
+// fa_fwd on planes [p0, p0 + H) of a B = 1 problem of `whole_planes` planes (the
+// host-buffer pipeline's chunks): the key split is chosen for the whole
+// problem, so the chunks' results equal fa_fwd's on the whole, bit for bit.
+int fwd_part(const void* q, const void* k, const void* v, void* o, float* lse, int H, int N, int D, float scale,
+             int causal, int dtype, long long whole_planes, cudaStream_t stream) {
+    CUtensorMap maps[3];
+    Params p;
+    const int st = prepare(q, k, v, o, lse, 1, H, H, N, N, D, scale, causal, dtype, 1, false, maps, p);
+    if (st != FA_OK) return st;
+    return dispatch<false>(maps, p, D, dtype, causal, stream, static_cast<long long>(p.n_qblocks) * whole_planes);
+}
+}  // namespace fa103
 
 extern "C" int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int H_kv,
                           int N, int D, float scale, int causal, int dtype, cudaStream_t stream) {

@@ -70,4 +70,10 @@ int bwd_take_status(unsigned int* bits);
 // The backward kernel's bit for "shared memory not laid out as required".
 constexpr unsigned int kBwdStatusLayout = 64u;
 
+// fa_fwd on H planes that are part of a B = 1 problem of `whole_planes` planes,
+// with the forward's form (256-row tiles or the key split) chosen for the whole
+// problem, so that per-part results equal the whole call's bit for bit.
+int fwd_part(const void* q, const void* k, const void* v, void* o, float* lse, int H, int N, int D, float scale,
+             int causal, int dtype, long long whole_planes, cudaStream_t stream);
+
 }  // namespace fa103

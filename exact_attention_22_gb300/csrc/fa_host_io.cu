@@ -210,9 +210,9 @@ extern "C" int fa_fwd_host(const void* q, const void* k, const void* v, void* o,
             status = FA_ERR_CUDA;
             break;
         }
-        status = fa_fwd(ws + off, ws + L.k + off, ws + L.v + off, ws + L.o + off,
-                        reinterpret_cast<float*>(ws + L.lse + loff), 1, static_cast<int>(np), N, D, scale, causal,
-                        dtype, stream);
+        status = fwd_part(ws + off, ws + L.k + off, ws + L.v + off, ws + L.o + off,
+                          reinterpret_cast<float*>(ws + L.lse + loff), static_cast<int>(np), N, D, scale, causal,
+                          dtype, planes, stream);
         ok = status == FA_OK && cudaEventRecord(io->out[c], stream) == cudaSuccess &&
              cudaStreamWaitEvent(io->d2h, io->out[c], 0) == cudaSuccess &&
              cudaMemcpyAsync(ho + off, ws + L.o + off, len, cudaMemcpyDeviceToHost, io->d2h) == cudaSuccess &&

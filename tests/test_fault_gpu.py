@@ -47,9 +47,13 @@ def _forward_matches_oracle(w, seed):
     assert float(np.abs(lse.cpu().numpy() - lse_ref).max()) <= 1e-3
 
 
+# The first two problems have fewer 256-row work tiles than SMs, so they run in
+# the key-split form (ring items of a work tile: K, V of stream 0's first K/V
+# tile, K, V of stream 1's first, then the second ones, ...); the third runs in
+# the 256-row form (K_0, V_0, K_1, V_1, ... shared by both streams).
 @pytest.mark.parametrize("B,H,N,D,causal,item", [
-    (1, 2, 1000, 64, True, 5),       # V_2 of the first work tile, P V of earlier steps in flight
-    (1, 2, 300, 128, False, 0),      # K_0: nothing issued yet when the wait runs out
+    (1, 2, 1000, 64, True, 5),       # V of stream 0's second K/V tile, P V of earlier steps in flight
+    (1, 2, 300, 128, False, 0),      # stream 0's first K: nothing issued yet when the wait runs out
     (1, 32, 2048, 128, True, 21),    # V_10 of the first work tile of some CTAs, V_0 or V_2 of the second of others
 ])
 def test_forward_gives_up_and_context_survives(B, H, N, D, causal, item):

@@ -94,6 +94,30 @@ def test_tiny_workload_elementwise():
     _check(o, lse, o_ref, lse_ref, w.dtype, what=w.name)
 
 
+# With no more 256-row work tiles than SMs, fa_fwd deals 128-row Q tiles whose
+# K/V tiles are shared out between the CTA's two streams (ceil(J/2) and
+# floor(J/2) of J) and merges the two partial (m, l, O) on chip.  These shapes
+# cover: a Q tile with one K/V tile (stream 1 has none), odd and even J, a ragged
+# last tile, grouped K/V heads, and the edge between the two forms on a 152-SM
+# GB300 (B1 H38 N1024: 152 tiles, key split; H39: 156 tiles, 256-row tiles).
+@pytest.mark.parametrize("B,H,H_kv,N,D,causal,dtype", [
+    (1, 4, 4, 129, 128, True, "fp16"),
+    (1, 3, 3, 640, 64, True, "bf16"),
+    (2, 5, 5, 1000, 128, False, "fp16"),
+    (1, 8, 2, 777, 64, True, "fp16"),
+    (1, 38, 38, 1024, 128, True, "fp16"),
+    (1, 39, 39, 1024, 128, True, "fp16"),
+])
+def test_key_split_and_its_edge_elementwise(B, H, H_kv, N, D, causal, dtype):
+    w = fa_inputs.Workload("ks", B, H, N, D, causal, dtype)
+    q, k, v = fa_inputs.make_qkv(w, seed=11)
+    k, v = k[:, :H_kv].contiguous(), v[:, :H_kv].contiguous()
+    o, lse = _run(q, k, v, causal, w.scale)
+    g = H // H_kv
+    o_ref, lse_ref = _oracle_full(q, k.repeat_interleave(g, dim=1), v.repeat_interleave(g, dim=1), causal, w.scale)
+    _check(o, lse, o_ref, lse_ref, dtype, what="B%d H%d/%d N%d D%d" % (B, H, H_kv, N, D))
+
+
 @pytest.mark.parametrize("B,H,N,D,causal,dtype", [
     (2, 32, 2048, 128, True, "fp16"),    # 512 work tiles: 3.4 rounds of the persistent grid
     (4, 16, 1024, 64, False, "bf16"),    # 256 work tiles, every CTA past its first round
