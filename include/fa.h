@@ -63,7 +63,11 @@ typedef enum {
  *
  * Returns FA_OK once the kernel is queued.  Argument errors are reported
  * before anything is launched and leave o / lse untouched.  N need not be a
- * multiple of any tile size.  Results are deterministic for fixed inputs.
+ * multiple of any tile size.  Results are deterministic for fixed inputs (and
+ * device): a launch with no more 256-row work tiles (ceil(N / 256) * B * H)
+ * than the device has SMs splits each 128-row query tile's keys between two
+ * partial softmax passes merged on chip, so its last bits can differ from the
+ * same rows computed inside a larger launch.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int D, float scale, int causal, int dtype,
