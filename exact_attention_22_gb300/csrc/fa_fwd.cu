@@ -146,7 +146,9 @@ struct Params {
 };
 
 // One work tile: query rows q0 .. q0+255 of head bh, K/V tiles j0 .. j0+n_all-1
-// (chunk `split` of the query block's range).
+// (chunk `split` of the query block's range).  In the key-split form (below):
+// query rows q0 .. q0+127 for both streams, stream 0 on K/V tiles 0 .. nkv[0]-1
+// and stream 1 on j0 .. j0+nkv[1]-1.
 struct Tile {
     int q0, bh, kvh, split, j0, n_all;   // kvh: K/V plane b * H_kv + h / kv_group
     int nkv[kNumQ];      // K/V tiles of this chunk each stream visits (0: none)
